@@ -1,0 +1,369 @@
+"""Benchmark of the indexer-Q preparation path on GB300.
+
+One step = one pass of the whole hot path over one batch: the FP8 1x128
+quantizer on the BF16 latent [4632, 1536], then the fused block-scaled FP8
+GEMM with the RoPE -> Hadamard -> FP4 epilogue, producing packed FP4 Q
+[4632, 4096] and its UE8M0 scales [4632, 256] (the two launches of
+iq_prepare_q).  Inputs are seeded synthetic data resident in HBM before the
+timed region; L2 is flushed (256 MB write) between timed steps, outside the
+CUDA-event intervals.  Also measured in the same run: the quantizer alone on
+BF16 [4632, 7168] (GB/s against HBM), the end-to-end call through
+iq_prepare_q with pinned host buffers (copies inside the timed region), and
+the CPU oracle on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs an independent replica on its own GPU (the
+path has no exchange step); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_PREFILL = 4632
+K_LATENT = 1536
+N_Q = 8192
+K_QUANT = 7168
+FLOPS_PER_TOKEN = 2 * N_Q * K_LATENT
+METRIC = "indexer-Q tokens/s at M=4632; FP8 quantizer GB/s vs HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 2.0            # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+ORACLE_SAMPLE_ROWS = 1024      # rows of the prefill workload per oracle timing
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                p = json.load(f)
+            hbm = p.get("hbm_gbs")
+            bf16 = p.get("bf16_tflops")
+            if hbm and bf16:
+                return float(hbm), float(bf16), "measured"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_traffic(kernel_key: str):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, or None
+    when the kernel's source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f).get(kernel_key)
+    if not t:
+        return None
+    src = os.path.join(ROOT, t["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != t["source_sha"]:
+        return None
+    return t["dram_bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi clocks sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def oracle_sample_seconds(rows: int) -> float:
+    """Times the CPU oracle (single thread) on the first `rows` tokens of the
+    prefill workload in a child process, so the BLAS thread count is pinned."""
+    code = (
+        "import os,sys,time; sys.path.insert(0, %r)\n"
+        "from fp4_fp8_quant_gb300 import workloads as W\n"
+        "from oracle import iq_oracle as O\n"
+        "x, wq, wsf, pos = W.prefill_chain(%d)\n"
+        "x, pos = x[:%d], pos[:%d]\n"
+        "t = time.perf_counter(); O.prepare_q(x, wq, wsf, pos); print(time.perf_counter() - t)\n"
+    ) % (ROOT, M_PREFILL, rows, rows)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, check=True)
+    return float(out.stdout.strip().splitlines()[-1])
+
+
+def run_reference(args):
+    """The oracle as it stands, on one host core, each step a 256-token sample
+    of the prefill workload."""
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    from fp4_fp8_quant_gb300 import workloads as W
+    from oracle import iq_oracle as O
+    rows = 256
+    x, wq, wsf, pos = W.prefill_chain(M_PREFILL)
+    for _ in range(args.warmup):
+        O.prepare_q(x[:rows], wq, wsf, pos[:rows])
+    times = []
+    for i in range(args.steps):
+        lo = (i * rows) % (M_PREFILL - rows)
+        t = time.perf_counter()
+        O.prepare_q(x[lo:lo + rows], wq, wsf, pos[lo:lo + rows])
+        times.append(time.perf_counter() - t)
+    per_step = sum(times) / len(times)
+    value = rows / per_step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "indexer-Q prefill chain, 4632 tokens x latent 1536 -> 64 heads x 128, "
+                               "positions 0..4631 (oracle: a 256-token slice per step)", "M": M_PREFILL},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "a 256-token slice of the 4632-token prefill workload per step, FP64 numpy, "
+                                   "one thread"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from fp4_fp8_quant_gb300 import build as B
+    B.build()
+    from fp4_fp8_quant_gb300 import iq, workloads as W
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush_l2():
+        flush_buf.fill_(rank & 0xFF)
+
+    # ---------------------------------------------------- the prefill chain
+    x, wq, wsf, pos = W.prefill_chain(M_PREFILL)
+    lat = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    w = torch.from_numpy(wq).to(dev)
+    ws = torch.from_numpy(wsf).to(dev)
+    p = torch.from_numpy(pos).to(dev)
+    M = M_PREFILL
+    xq = torch.empty((M, K_LATENT), dtype=torch.uint8, device=dev)
+    xs = torch.empty((3, (M + 3) // 4 * 4), dtype=torch.int32, device=dev)
+    q = torch.empty((M, N_Q // 2), dtype=torch.uint8, device=dev)
+    s = torch.empty((M, N_Q // 32), dtype=torch.uint8, device=dev)
+
+    def step():
+        iq.fp8_quant_1x128_ue8m0(lat, y=xq, scales=xs)
+        iq.gemm_rope_hadamard_fp4(xq, xs, w, ws, p, q_fp4=q, q_sf=s)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush_l2()
+            ev[i][0].record(stream)
+            iq.fp8_quant_1x128_ue8m0(lat, y=xq, scales=xs)
+            ev[i][1].record(stream)
+            iq.gemm_rope_hadamard_fp4(xq, xs, w, ws, p, q_fp4=q, q_sf=s)
+            ev[i][2].record(stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    k1_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    k2_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    my_ms = sum(step_ms) / len(step_ms)
+    t = torch.tensor([my_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_per_step = float(t.item())
+    value = world * M / (ms_per_step * 1e-3)
+    k2_avg_ms = sum(k2_ms) / len(k2_ms)
+
+    hbm_peak, bf16_peak, peak_kind = load_peaks()
+    fp8_peak_tflops = bf16_peak * FP8_OVER_BF16
+    achieved_tflops = M * FLOPS_PER_TOKEN / (k2_avg_ms * 1e-3) / 1e12
+    roofline = {"kernel": "gemm_rope_hadamard_fp4_kernel", "bound": "tensor", "achieved": achieved_tflops,
+                "peak": fp8_peak_tflops, "unit": "TFLOP/s", "frac": achieved_tflops / fp8_peak_tflops,
+                "traffic": kernel_traffic("gemm_rope_hadamard_fp4_kernel"),
+                "peak_source": f"{peak_kind} bf16 x {FP8_OVER_BF16:g} (FP8/BF16 nominal ratio)",
+                "avg_launch_ms": k2_avg_ms, "flops_per_launch": M * FLOPS_PER_TOKEN}
+
+    # ------------------------------------------------- the quantizer alone
+    xb = W.quant_blocks_input(M_PREFILL, K_QUANT, seed=1)
+    X = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
+    Y = torch.empty((M_PREFILL, K_QUANT), dtype=torch.uint8, device=dev)
+    S = torch.empty(((K_QUANT + 511) // 512, (M_PREFILL + 3) // 4 * 4), dtype=torch.int32, device=dev)
+    for _ in range(3):
+        iq.fp8_quant_1x128_ue8m0(X, y=Y, scales=S)
+    torch.cuda.synchronize()
+    qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in qev:
+        flush_l2()
+        a.record(stream)
+        iq.fp8_quant_1x128_ue8m0(X, y=Y, scales=S)
+        b.record(stream)
+    torch.cuda.synchronize()
+    q_ms = sum(a.elapsed_time(b) for a, b in qev) / len(qev)
+    q_bytes = M_PREFILL * K_QUANT * 3 + S.numel() * 4
+    q_gbs = q_bytes / (q_ms * 1e-3) / 1e9
+    quantizer = {"workload": "BF16 [4632, 7168] -> E4M3 + packed UE8M0 scales", "value": q_gbs, "unit": "GB/s",
+                 "avg_launch_ms": q_ms,
+                 "roofline": {"kernel": "quant_1x128_kernel", "bound": "hbm", "achieved": q_gbs, "peak": hbm_peak,
+                              "unit": "GB/s", "frac": q_gbs / hbm_peak, "traffic": kernel_traffic("quant_1x128_kernel"),
+                              "peak_source": peak_kind, "bytes_per_launch": q_bytes}}
+
+    # ------------------------------------------ end to end through the C ABI
+    h_lat = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_pos = torch.from_numpy(pos).pin_memory()
+    h_q = torch.empty((M, N_Q // 2), dtype=torch.uint8).pin_memory()
+    h_s = torch.empty((M, N_Q // 32), dtype=torch.uint8).pin_memory()
+    d_lat = torch.empty_like(lat)
+    d_pos = torch.empty_like(p)
+    work = torch.empty(iq.prepare_q_workspace_bytes(M), dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        d_lat.copy_(h_lat, non_blocking=True)
+        d_pos.copy_(h_pos, non_blocking=True)
+        iq.prepare_q(d_lat, w, ws, d_pos, q_fp4=q, q_sf=s, workspace=work)
+        h_q.copy_(q, non_blocking=True)
+        h_s.copy_(s, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in eev:
+        flush_l2()
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / len(eev)
+    e2e = {"value": world * M / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": h_lat.numel() * 2 + h_pos.numel() * 4,
+           "d2h_bytes_per_step": h_q.numel() + h_s.numel()}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs = oracle_sample_seconds(ORACLE_SAMPLE_ROWS)
+        cpu = {"value": ORACLE_SAMPLE_ROWS / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {ORACLE_SAMPLE_ROWS} tokens of the 4632-token prefill workload, FP64 numpy, "
+                         f"one thread ({secs:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3xe4m3->f32, e2m1 out", "data": "synthetic",
+            "config": {"workload": "indexer-Q prefill chain: BF16 latent [4632, 1536] (N(0,1), 0.1% outliers x50) "
+                                   "-> FP8 1x128 quantize -> block-scaled FP8 GEMM with W_q [8192, 1536] -> NeoX "
+                                   "RoPE (positions 0..4631) -> Hadamard-128 -> MXFP4 [4632, 4096] + UE8M0 "
+                                   "[4632, 256]",
+                       "M": M, "K": K_LATENT, "N": N_Q, "parallelism": f"replicas x{world}",
+                       "l2": "flushed (256 MB write) between timed steps, outside the event intervals"},
+            "roofline": roofline, "quantizer": quantizer, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks.summary(),
+            "k1_chain_avg_ms": sum(k1_ms) / len(k1_ms), "wall_s_timed": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

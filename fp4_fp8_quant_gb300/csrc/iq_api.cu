@@ -1,0 +1,240 @@
+// C-ABI entry points of the indexer-Q preparation library (include/iq.h):
+// argument checks, per-device set-up, TMA descriptor encoding and launches.
+// Nothing here allocates device memory or synchronizes a stream.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "iq.h"
+#include "iq_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+struct DeviceInfo {
+  bool ready = false;
+  iq_status status = IQ_OK;
+  int num_sms = 0;
+};
+
+std::mutex g_setup_mutex;
+DeviceInfo g_devices[kMaxDevices];
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// First call on a device: check the architecture, set kernel attributes and
+// resolve the driver's tensor-map encoder.  Later calls only read the cache.
+iq_status device_setup(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return IQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      return IQ_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) {
+      d.status = IQ_ERR_ARCH;
+    } else if (iq::gemm_setup_device() != cudaSuccess) {
+      d.status = IQ_ERR_CUDA;
+    } else {
+      d.status = IQ_OK;
+    }
+    if (d.status == IQ_OK && g_encode_tiled == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        d.status = IQ_ERR_CUDA;
+      } else {
+        g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      }
+    }
+    d.num_sms = sms;
+    d.ready = true;
+  }
+  *num_sms = d.num_sms;
+  return d.status;
+}
+
+// 2D uint8 tensor map, inner dimension K bytes, 128-byte swizzled boxes.
+bool encode_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                  uint32_t box_rows) {
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+iq::RopeTurns make_rope_turns() {
+  iq::RopeTurns t;
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < 32; ++i) {
+    const double g = std::pow(10000.0, -static_cast<double>(i) / 32.0) / two_pi;
+    t.hi[i] = static_cast<float>(g);
+    t.lo[i] = static_cast<float>(g - static_cast<double>(t.hi[i]));
+  }
+  return t;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq, const uint8_t* wq_sf,
+                     const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf, float* q_pre, int num_sms,
+                     cudaStream_t stream) {
+  static const iq::RopeTurns rope = make_rope_turns();
+  CUtensorMap tm_x, tm_w;
+  if (!encode_2d_u8(&tm_x, xq, iq::kLatentDim, static_cast<uint64_t>(M), 128, 128) ||
+      !encode_2d_u8(&tm_w, wq, iq::kLatentDim, iq::kQDim, 128, 256)) {
+    return IQ_ERR_CUDA;
+  }
+  iq::GemmArgs a;
+  a.x_sf = x_sf;
+  a.w_sf = wq_sf;
+  a.pos = positions;
+  a.q_fp4 = q_fp4;
+  a.q_sf = q_sf;
+  a.q_pre = q_pre;
+  a.M = M;
+  a.m_al = (M + 3) / 4 * 4;
+  a.num_m_tiles = (M + 127) / 128;
+  a.num_tiles = a.num_m_tiles * (iq::kQDim / 256);
+  a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  a.rope = rope;
+  return iq::launch_gemm_rope_hadamard_fp4(tm_x, tm_w, a, num_sms, stream) == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
+}
+
+iq_status check_prepare_args(const void* latent, int M, const void* wq, const uint8_t* wq_sf, const int32_t* pos,
+                             uint8_t* q_fp4, uint8_t* q_sf, const float* q_pre, bool need_pre) {
+  if (M < 0) return IQ_ERR_ARG;
+  if (M == 0) return IQ_OK;
+  if (!latent || !wq || !wq_sf || !pos || !q_fp4 || !q_sf || (need_pre && !q_pre)) return IQ_ERR_ARG;
+  if (!aligned(latent, 16) || !aligned(wq, 16) || !aligned(pos, 4) || !aligned(q_fp4, 16) || !aligned(q_sf, 4) ||
+      (q_pre && !aligned(q_pre, 16))) {
+    return IQ_ERR_ALIGN;
+  }
+  return IQ_OK;
+}
+
+iq_status prepare_impl(const void* latent, int M, const void* wq, const uint8_t* wq_sf, const int32_t* pos,
+                       uint8_t* q_fp4, uint8_t* q_sf, float* q_pre, bool need_pre, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  iq_status st = check_prepare_args(latent, M, wq, wq_sf, pos, q_fp4, q_sf, q_pre, need_pre);
+  if (st != IQ_OK || M == 0) return st;
+  if (!ws) return IQ_ERR_ARG;
+  if (!aligned(ws, 256)) return IQ_ERR_ALIGN;
+  if (ws_bytes < iq_prepare_q_workspace(M)) return IQ_ERR_WORKSPACE;
+  int num_sms = 0;
+  st = device_setup(&num_sms);
+  if (st != IQ_OK) return st;
+  uint8_t* xq = static_cast<uint8_t*>(ws);
+  int32_t* x_sf = reinterpret_cast<int32_t*>(xq + align_up(static_cast<size_t>(M) * iq::kLatentDim, 256));
+  if (iq::launch_quant_1x128(latent, M, iq::kLatentDim, iq::kLatentDim, xq, iq::kLatentDim, x_sf, stream) !=
+      cudaSuccess) {
+    return IQ_ERR_CUDA;
+  }
+  return gemm_stage(xq, x_sf, M, wq, wq_sf, pos, q_fp4, q_sf, q_pre, num_sms, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* iq_status_str(iq_status s) {
+  switch (s) {
+    case IQ_OK: return "IQ_OK";
+    case IQ_ERR_ARG: return "IQ_ERR_ARG: null pointer or invalid size";
+    case IQ_ERR_ALIGN: return "IQ_ERR_ALIGN: pointer or leading dimension not aligned";
+    case IQ_ERR_SHAPE: return "IQ_ERR_SHAPE: K must be positive and a multiple of 128";
+    case IQ_ERR_ARCH: return "IQ_ERR_ARCH: device is not sm_103 (GB300)";
+    case IQ_ERR_CUDA: return "IQ_ERR_CUDA: CUDA runtime or launch failure";
+    case IQ_ERR_WORKSPACE: return "IQ_ERR_WORKSPACE: workspace too small";
+    case IQ_ERR_TIMEOUT: return "IQ_ERR_TIMEOUT: a device-side wait gave up";
+  }
+  return "unknown iq_status";
+}
+
+iq_status iq_device_status(uint32_t* flags, int reset) {
+  uint32_t v = 0;
+  if (iq::read_device_status(&v, reset != 0) != cudaSuccess) return IQ_ERR_CUDA;
+  if (flags) *flags = v;
+  return v ? IQ_ERR_TIMEOUT : IQ_OK;
+}
+
+void iq_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs); }
+
+size_t iq_fp8_scale_words(int M, int K) {
+  if (M <= 0 || K <= 0) return 0;
+  return static_cast<size_t>((K + 511) / 512) * align_up(static_cast<size_t>(M), 4);
+}
+
+iq_status iq_fp8_quant_1x128_ue8m0(const void* x_bf16, int M, int K, int ldx, void* y_e4m3, int ldy,
+                                   int32_t* scales, cudaStream_t stream) {
+  if (M < 0) return IQ_ERR_ARG;
+  if (K <= 0 || K % 128 != 0) return IQ_ERR_SHAPE;
+  if (M == 0) return IQ_OK;
+  if (!x_bf16 || !y_e4m3 || !scales) return IQ_ERR_ARG;
+  if (ldx < K || ldy < K) return IQ_ERR_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(y_e4m3, 16) || !aligned(scales, 4) || ldx % 8 != 0 || ldy % 16 != 0) {
+    return IQ_ERR_ALIGN;
+  }
+  int num_sms = 0;
+  const iq_status st = device_setup(&num_sms);
+  if (st != IQ_OK) return st;
+  return iq::launch_quant_1x128(x_bf16, M, K, ldx, y_e4m3, ldy, scales, stream) == cudaSuccess ? IQ_OK
+                                                                                                : IQ_ERR_CUDA;
+}
+
+size_t iq_prepare_q_workspace(int M) {
+  if (M <= 0) return 0;
+  return align_up(static_cast<size_t>(M) * iq::kLatentDim, 256) +
+         static_cast<size_t>(iq::kScaleGroups) * align_up(static_cast<size_t>(M), 4) * sizeof(int32_t);
+}
+
+iq_status iq_prepare_q(const void* latent_bf16, int M, const void* wq_e4m3, const uint8_t* wq_sf,
+                       const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf, void* workspace, size_t ws_bytes,
+                       cudaStream_t stream) {
+  return prepare_impl(latent_bf16, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, nullptr, false, workspace, ws_bytes,
+                      stream);
+}
+
+iq_status iq_prepare_q_debug(const void* latent_bf16, int M, const void* wq_e4m3, const uint8_t* wq_sf,
+                             const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf, float* q_prequant,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return prepare_impl(latent_bf16, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, q_prequant, true, workspace, ws_bytes,
+                      stream);
+}
+
+iq_status iq_gemm_rope_hadamard_fp4(const void* xq_e4m3, const int32_t* x_scales, int M, const void* wq_e4m3,
+                                    const uint8_t* wq_sf, const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf,
+                                    float* q_prequant, cudaStream_t stream) {
+  iq_status st = check_prepare_args(xq_e4m3, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, q_prequant, false);
+  if (st != IQ_OK || M == 0) return st;
+  if (!x_scales) return IQ_ERR_ARG;
+  if (!aligned(x_scales, 4)) return IQ_ERR_ALIGN;
+  int num_sms = 0;
+  st = device_setup(&num_sms);
+  if (st != IQ_OK) return st;
+  return gemm_stage(xq_e4m3, x_scales, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, q_prequant, num_sms, stream);
+}
+
+}  // extern "C"

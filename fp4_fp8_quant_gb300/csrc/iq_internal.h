@@ -1,0 +1,66 @@
+// Internal declarations shared by the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace iq {
+
+// Tiny-amax floor of both block quantizers (the "tiny-scale floor" of the
+// TokenSpeed PR, Risk and fallback): blocks whose largest magnitude is below it
+// take the scale exponent of the floor.
+constexpr float kAmaxFloor = 1e-4f;
+
+constexpr int kLatentDim = 1536;
+constexpr int kNumHeads = 64;
+constexpr int kHeadDim = 128;
+constexpr int kQDim = kNumHeads * kHeadDim;   // 8192
+constexpr int kNumKBlocks = kLatentDim / 128; // 12
+constexpr int kScaleGroups = kNumKBlocks / 4; // 3 packed int32 words per row
+
+// RoPE frequencies of the 32 NeoX pairs, in turns per position unit:
+// 10000^(-i/32) / (2 pi), split into a float32 head and tail.
+struct RopeTurns {
+  float hi[32];
+  float lo[32];
+};
+
+struct GemmArgs {
+  const int32_t* x_sf;   // [3][m_al] packed UE8M0 words of the FP8 latent
+  const uint8_t* w_sf;   // [64][12] UE8M0 bytes of the weight blocks
+  const int32_t* pos;    // [M]
+  uint8_t* q_fp4;        // [M][4096]
+  uint8_t* q_sf;         // [M][256]
+  float* q_pre;          // [M][8192] or nullptr
+  int M;
+  int m_al;
+  int num_m_tiles;
+  int num_tiles;
+  unsigned long long timeout_ns;
+  RopeTurns rope;
+};
+
+// Status bits of the device status word (which wait gave up).
+enum : uint32_t {
+  kStatusProducerWait = 1u << 0,
+  kStatusMmaWait = 1u << 1,
+  kStatusEpilogueWait = 1u << 2,
+  kStatusTeardownWait = 1u << 3,
+};
+
+cudaError_t launch_quant_1x128(const void* x, int M, int K, long long ldx, void* y, long long ldy, int32_t* sf,
+                               cudaStream_t stream);
+
+// Kernel attribute set-up of the fused GEMM on the current device.
+cudaError_t gemm_setup_device();
+int gemm_smem_bytes();
+
+cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const GemmArgs& args,
+                                          int num_sms, cudaStream_t stream);
+
+// Device status word access (synchronous).
+cudaError_t read_device_status(uint32_t* flags, bool reset);
+
+}  // namespace iq

@@ -1,0 +1,179 @@
+/*
+ * iq.h -- C ABI of the GB300 (sm_103a) DeepSeek-V4 indexer-Q preparation path.
+ *
+ * Two operations, each an asynchronous launch sequence on a caller stream:
+ *
+ *  1. iq_fp8_quant_1x128_ue8m0: the packed-UE8M0 FP8 online activation
+ *     quantizer of the TokenSpeed PR "perf(deepseek-v4): accelerate indexer Q
+ *     and packed FP8 quantization" (Summary; Risk and fallback: contiguous,
+ *     aligned BF16 input, K divisible by 128, the packed-UE8M0 scale contract
+ *     and the tiny-scale floor), which the TensorRT-LLM PR "Fuse DeepSeek-V4
+ *     Indexer Q projection with CuTe DSL" calls fp8_quantize_1x128 with UE8M0
+ *     scales (Walkthrough / sequence diagram).
+ *
+ *  2. iq_prepare_q: the fused indexer-Q projection of the TensorRT-LLM PR
+ *     (sequence diagram: FP8 input and UE8M0 scales, block-scaled GEMM "with
+ *     RoPE and FP4 epilogue", packed FP4 Q and scales returned; review comment
+ *     on the fused epilogue: MXF8 scale vector 32, one 128-column head per MMA
+ *     tile) with the Hadamard transform that the TokenSpeed PR applies to the
+ *     indexer Q (Summary; Main-rebase compatibility fix).
+ *
+ * Numbers used throughout (element formats per the OCP FP8 / MX specs):
+ *   E4M3: FP8 with 4 exponent bits (bias 7), 3 mantissa bits, max 448.
+ *   E2M1: FP4 with 2 exponent bits (bias 1), 1 mantissa bit, max 6.
+ *   UE8M0: unsigned 8-bit exponent; byte b encodes 2^(b - 127).
+ *   Block scale exponent of a block with largest magnitude a:
+ *       e = smallest integer with qmax * 2^e >= max(a, 1e-4)   (qmax 448 or 6)
+ *   Element code = round-to-nearest-even(x * 2^-e) in the element format.
+ *
+ * Memory: the caller owns every buffer (inputs, outputs, workspace).  No call
+ * allocates device memory, synchronizes the device or the stream, or falls
+ * back to another implementation.  Pointers are device pointers unless stated.
+ * All calls are asynchronous on `stream`; errors detected on the host are
+ * returned before anything is launched.  A return of IQ_OK means the launches
+ * were enqueued; a device-side wait that ran out of time is recorded in the
+ * device status word (iq_device_status).
+ *
+ * Thread safety: calls may be made from several host threads; the only shared
+ * host state is the per-device set-up done on the first call on a device
+ * (architecture check, kernel attributes), which is guarded.
+ */
+#ifndef IQ_H_
+#define IQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  IQ_OK = 0,
+  IQ_ERR_ARG = -1,        /* null pointer, M < 0, bad leading dimension */
+  IQ_ERR_ALIGN = -2,      /* a pointer or leading dimension breaks the alignment rule */
+  IQ_ERR_SHAPE = -3,      /* K <= 0 or K % 128 != 0 */
+  IQ_ERR_ARCH = -4,       /* current device is not compute capability 10.3 (sm_103) */
+  IQ_ERR_CUDA = -5,       /* a CUDA runtime call or launch failed */
+  IQ_ERR_WORKSPACE = -6,  /* workspace smaller than iq_prepare_q_workspace(M) */
+  IQ_ERR_TIMEOUT = -7     /* a device-side wait gave up (see iq_device_status) */
+} iq_status;
+
+/* Human-readable name of a status code (static storage). */
+const char* iq_status_str(iq_status s);
+
+/* Device-side status word of the current device: bit i set means a wait of
+ * kind i ran out of time in some launch since the last reset.  Reads it into
+ * *flags (may be NULL) and clears it when `reset` is nonzero.  This call
+ * synchronizes with the device (it copies from device memory); it is a
+ * diagnostic, not part of the hot path.  Returns IQ_ERR_TIMEOUT when the word
+ * was nonzero, IQ_OK otherwise. */
+iq_status iq_device_status(uint32_t* flags, int reset);
+
+/* Overrides the time after which a device-side wait gives up, in nanoseconds
+ * (default 2e9).  0 restores the default.  Applies to later launches from any
+ * thread. */
+void iq_set_wait_timeout_ns(uint64_t ns);
+
+/* ------------------------------------------------------------------------
+ * 1. FP8 1x128 quantizer with packed UE8M0 scales.
+ * ------------------------------------------------------------------------ */
+
+/* Number of int32 scale words the quantizer writes for an M x K input:
+ * ceil(K / 512) * align_up(M, 4).  Returns 0 when M <= 0 or K <= 0. */
+size_t iq_fp8_scale_words(int M, int K);
+
+/* Quantizes x (BF16, row-major [M, ldx], first K columns used) per row and
+ * per 1x128 block:
+ *   y[m, k]   = E4M3 code of x[m, k] * 2^-e(m, k/128)        (row-major [M, ldy])
+ *   scales    = int32 words [ceil(K/512)][align_up(M, 4)] (M-major, the
+ *               TMA-aligned layout a DeepGEMM-style consumer reads):
+ *               byte j (little-endian) of word [g][m] is the UE8M0 scale byte
+ *               e + 127 of block 4g + j of row m; bytes of blocks past K/128
+ *               and words of rows m >= M are written as 0.
+ * The sign of zero is kept (-0 and values that round to zero from below give
+ * code 0x80).  NaN or infinite inputs are outside the contract.
+ * Requirements: M >= 0; K > 0 and K % 128 == 0 (else IQ_ERR_SHAPE);
+ *   ldx >= K, ldy >= K; x and y 16-byte aligned, ldx % 8 == 0 and
+ *   ldy % 16 == 0, scales 4-byte aligned (else IQ_ERR_ALIGN).
+ * M == 0 returns IQ_OK without a launch.  One kernel launch. */
+iq_status iq_fp8_quant_1x128_ue8m0(const void* x_bf16, int M, int K, int ldx,
+                                   void* y_e4m3, int ldy, int32_t* scales,
+                                   cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * 2. Indexer-Q preparation: FP8 quantize -> block-scaled FP8 GEMM -> RoPE ->
+ *    Hadamard-128 -> FP4 (E2M1) with 1x32 UE8M0 scales.
+ *
+ * Fixed shapes: latent dimension K = 1536; Q has 64 heads of 128 dims
+ * (N = 8192).  Per token m and head h (n = 128 h + d):
+ *   Y[m, n] = sum_kb 2^(eX[m,kb] + eW[h,kb]) * sum_{k in kb} x[m,k] w[n,k]
+ *             over 12 blocks kb of 128, x the E4M3 latent codes (operation 1
+ *             applied to the BF16 latent), w the weight codes;
+ *   RoPE:     NeoX rotation of dims d = 0..63 in pairs (i, i+32) by the angle
+ *             position[m] * 10000^(-i/32); dims 64..127 unchanged;
+ *   Hadamard: z = H r / sqrt(128), H[i][j] = (-1)^popcount(i & j);
+ *   FP4:      per block of 32 consecutive dims, e from qmax 6, codes
+ *             E2M1(z * 2^-e) with the sign of zero kept.
+ * The pre-quant Q (z) is kept in float32 and is never rounded to BF16.
+ * ------------------------------------------------------------------------ */
+
+#define IQ_LATENT_DIM 1536
+#define IQ_NUM_HEADS 64
+#define IQ_HEAD_DIM 128
+#define IQ_Q_DIM 8192
+
+/* Workspace bytes iq_prepare_q needs for M tokens: the E4M3 latent
+ * [M, 1536] at offset 0 followed, at the next 256-byte boundary, by its packed
+ * scale words [3][align_up(M, 4)].  Returns 0 when M <= 0. */
+size_t iq_prepare_q_workspace(int M);
+
+/* Arguments:
+ *   latent_bf16  [M, 1536] BF16, contiguous, 16-byte aligned.
+ *   wq_e4m3      [8192, 1536] E4M3 codes, row-major (row n = output feature n),
+ *                16-byte aligned.
+ *   wq_sf        [64][12] UE8M0 bytes, row-major: scale of the 128x128 weight
+ *                block (head h, K-block kb).
+ *   positions    [M] int32 token positions (any value with |p| < 2^24).
+ *   q_fp4        [M, 4096] bytes, 16-byte aligned: byte 64 h + 16 b + i of
+ *                row m holds dims 32 b + 2i (low nibble) and 32 b + 2i + 1
+ *                (high nibble) of head h.
+ *   q_sf         [M, 256] UE8M0 bytes, 4-byte aligned: byte 4 h + b is the
+ *                scale of block b of head h.
+ *   workspace    caller scratch of at least iq_prepare_q_workspace(M) bytes,
+ *                256-byte aligned; its contents on return are the FP8 latent
+ *                and its packed scales (operation 1's outputs).
+ * M == 0 returns IQ_OK without a launch.  Two kernel launches (the quantizer
+ * and the fused GEMM), back to back on `stream`. */
+iq_status iq_prepare_q(const void* latent_bf16, int M,
+                       const void* wq_e4m3, const uint8_t* wq_sf,
+                       const int32_t* positions,
+                       uint8_t* q_fp4, uint8_t* q_sf,
+                       void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* iq_prepare_q that also writes the float32 pre-quant Q (z above) to
+ * q_prequant [M, 8192] (row-major, 16-byte aligned). */
+iq_status iq_prepare_q_debug(const void* latent_bf16, int M,
+                             const void* wq_e4m3, const uint8_t* wq_sf,
+                             const int32_t* positions,
+                             uint8_t* q_fp4, uint8_t* q_sf, float* q_prequant,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* The second stage alone, for callers that already hold the FP8 latent and its
+ * packed scales (the outputs of operation 1 with K = 1536):
+ *   xq_e4m3      [M, 1536] E4M3 codes, contiguous, 16-byte aligned.
+ *   x_scales     [3][align_up(M, 4)] packed UE8M0 words, 4-byte aligned.
+ *   q_prequant   may be NULL; otherwise as in iq_prepare_q_debug.
+ * One kernel launch. */
+iq_status iq_gemm_rope_hadamard_fp4(const void* xq_e4m3, const int32_t* x_scales, int M,
+                                    const void* wq_e4m3, const uint8_t* wq_sf,
+                                    const int32_t* positions,
+                                    uint8_t* q_fp4, uint8_t* q_sf, float* q_prequant,
+                                    cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IQ_H_ */

@@ -1,0 +1,82 @@
+"""The C ABI: the library builds, loads without a GPU, exports every function
+include/iq.h declares, and its host-side checks and size helpers behave as
+documented (none of these calls touches a device)."""
+
+import os
+import re
+import subprocess
+
+import pytest
+
+from fp4_fp8_quant_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "iq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(iq_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    from fp4_fp8_quant_gb300 import iq
+    return iq.lib()
+
+
+def test_header_declarations_match_binding(lib):
+    from fp4_fp8_quant_gb300 import iq
+    assert _declared_functions() == sorted(iq.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(iq_[a-z0-9_]+)$", out, flags=re.M))
+    missing = [f for f in _declared_functions() if f not in exported]
+    assert not missing, missing
+    for f in _declared_functions():
+        assert getattr(lib, f) is not None
+
+
+def test_size_helpers(lib):
+    assert lib.iq_fp8_scale_words(4632, 7168) == 14 * 4632
+    assert lib.iq_fp8_scale_words(5, 1536) == 3 * 8
+    assert lib.iq_fp8_scale_words(5, 640) == 2 * 8
+    assert lib.iq_fp8_scale_words(0, 1536) == 0
+    assert lib.iq_prepare_q_workspace(4632) == 4632 * 1536 + 3 * 4632 * 4
+    assert lib.iq_prepare_q_workspace(5) == 7680 + 3 * 8 * 4
+    assert lib.iq_prepare_q_workspace(0) == 0
+
+
+def test_host_side_argument_checks_need_no_device(lib):
+    # shape and argument errors are returned before any CUDA call
+    assert lib.iq_fp8_quant_1x128_ue8m0(16, 4, 200, 256, 16, 256, 16, None) == -3
+    assert lib.iq_fp8_quant_1x128_ue8m0(16, 4, 0, 256, 16, 256, 16, None) == -3
+    assert lib.iq_fp8_quant_1x128_ue8m0(16, -1, 128, 256, 16, 256, 16, None) == -1
+    assert lib.iq_fp8_quant_1x128_ue8m0(16, 0, 128, 256, 16, 256, 16, None) == 0
+    assert lib.iq_fp8_quant_1x128_ue8m0(None, 4, 128, 256, 16, 256, 16, None) == -1
+    assert lib.iq_fp8_quant_1x128_ue8m0(18, 4, 128, 256, 16, 256, 16, None) == -2
+    assert lib.iq_fp8_quant_1x128_ue8m0(16, 4, 128, 100, 16, 256, 16, None) == -1
+    assert lib.iq_prepare_q(16, 0, 16, 16, 16, 16, 16, None, 0, None) == 0
+    assert lib.iq_prepare_q(16, -3, 16, 16, 16, 16, 16, None, 0, None) == -1
+    assert lib.iq_prepare_q(16, 4, 16, 16, 16, 16, 16, None, 0, None) == -1
+    assert lib.iq_prepare_q(16, 4, 16, 16, 16, 16, 16, 256, 10, None) == -6
+    assert lib.iq_prepare_q(16, 4, 17, 16, 16, 16, 16, 256, 1 << 20, None) == -2
+    assert lib.iq_prepare_q_debug(16, 4, 16, 16, 16, 16, 16, None, 256, 1 << 20, None) == -1
+    assert lib.iq_gemm_rope_hadamard_fp4(16, None, 4, 16, 16, 16, 16, 16, None, None) == -1
+
+
+def test_status_strings(lib):
+    for code in range(0, -8, -1):
+        s = lib.iq_status_str(code).decode()
+        assert s.startswith("IQ_")
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from fp4_fp8_quant_gb300 import iq
+    monkeypatch.setattr(iq, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(iq, "_lib", None)
+    with pytest.raises(ImportError):
+        iq.lib()
