@@ -15,7 +15,9 @@
       rounding midpoint between the two codes; a sign difference of a value
       that rounds to zero counts as a step across the zero boundary and needs
       |u| <= 6e-4 (1e-4 of the FP4 range);
-    - at least 99.99% of all elements are equal.
+    - at least 99.99% of all elements are equal, where +0 and -0 (codes 0x0
+      and 0x8, the same value) count as equal: the sign of an exact zero
+      depends on the order of the additions that produced it.
 """
 
 from __future__ import annotations
@@ -99,6 +101,7 @@ def check_fp4(gpu_q, gpu_sf, ora_q, ora_sf, ora_z, min_equal=0.9999):
     same = ~sf_diff
     diff = (gc != oc) & same[..., None]
     n_code = int(diff.sum())
+    n_zero_flip = 0
     worst_rel = 0.0
     if n_code:
         mi, bi, ji = np.nonzero(diff)
@@ -116,9 +119,12 @@ def check_fp4(gpu_q, gpu_sf, ora_q, ora_sf, ora_z, min_equal=0.9999):
         dist = np.where(step_ok, np.abs(np.abs(u) - mid) / np.maximum(mid, 1e-300), np.abs(u) / 6.0)
         worst_rel = float(dist.max())
         assert np.all(dist <= 1e-4), f"FP4 code mismatch {worst_rel:.3g} away from a rounding boundary"
+        n_zero_flip = int(zero_flip.sum())
+        n_code -= int(zero_flip.sum())
     n_mis += n_code
     total = gc.size
     frac_equal = 1.0 - n_mis / max(total, 1)
     assert frac_equal >= min_equal, f"only {frac_equal:.6f} of FP4 codes equal"
     return {"scale_mismatch_blocks": int(sf_diff.sum()), "code_mismatches": n_code,
+            "signed_zero_flips": n_zero_flip,
             "equal_fraction": frac_equal, "worst_boundary_rel": worst_rel}
