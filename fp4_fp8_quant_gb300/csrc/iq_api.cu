@@ -238,3 +238,59 @@ iq_status iq_gemm_rope_hadamard_fp4(const void* xq_e4m3, const int32_t* x_scales
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// iq_prepare_q_static: the indexer-Q preparation for callers that cannot
+// allocate device memory.  The FP8 latent and its scale words go to a scratch
+// array compiled into the library instead of a caller workspace.
+
+namespace {
+
+constexpr size_t kStaticLatentBytes = static_cast<size_t>(IQ_STATIC_MAX_TOKENS) * iq::kLatentDim;
+constexpr size_t kStaticScratchBytes =
+    (kStaticLatentBytes + 255) / 256 * 256 + static_cast<size_t>(iq::kScaleGroups) * IQ_STATIC_MAX_TOKENS * 4;
+
+// One scratch array per device, alive until the process exits.
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mutex;
+void* g_static_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name stands for a host-side shadow, not device memory, so the
+// address is looked up once per device (with that device current) and cached.
+iq_status static_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return IQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (g_static_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return IQ_ERR_CUDA;
+    g_static_scratch_addr[dev] = p;
+  }
+  *out = g_static_scratch_addr[dev];
+  return IQ_OK;
+}
+
+}  // namespace
+
+extern "C" iq_status iq_prepare_q_static(const void* latent_bf16, int M, const void* wq_e4m3, const uint8_t* wq_sf,
+                                         const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf,
+                                         cudaStream_t stream) {
+  iq_status st = check_prepare_args(latent_bf16, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, nullptr, false);
+  if (st != IQ_OK || M == 0) return st;
+  if (M > IQ_STATIC_MAX_TOKENS) return IQ_ERR_WORKSPACE;
+  int num_sms = 0;
+  st = device_setup(&num_sms);
+  if (st != IQ_OK) return st;
+  void* scratch = nullptr;
+  st = static_scratch_address(&scratch);
+  if (st != IQ_OK) return st;
+  uint8_t* xq = static_cast<uint8_t*>(scratch);
+  int32_t* x_sf = reinterpret_cast<int32_t*>(xq + align_up(static_cast<size_t>(M) * iq::kLatentDim, 256));
+  if (iq::launch_quant_1x128(latent_bf16, M, iq::kLatentDim, iq::kLatentDim, xq, iq::kLatentDim, x_sf, stream) !=
+      cudaSuccess) {
+    return IQ_ERR_CUDA;
+  }
+  return gemm_stage(xq, x_sf, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, nullptr, num_sms, stream);
+}

@@ -36,6 +36,7 @@ SIGNATURES = {
     "iq_prepare_q": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "iq_prepare_q_debug": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "iq_gemm_rope_hadamard_fp4": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "iq_prepare_q_static": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
 }
 
 _lib = None

@@ -172,6 +172,42 @@ iq_status iq_gemm_rope_hadamard_fp4(const void* xq_e4m3, const int32_t* x_scales
                                     uint8_t* q_fp4, uint8_t* q_sf, float* q_prequant,
                                     cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Indexer-Q preparation without any device allocation.  The pages have no
+ * counterpart of this call; it exists for callers that cannot obtain device
+ * memory at the point where they prepare Q -- for example a plugin whose host
+ * program owns every device allocation and offers it no allocator, or a
+ * latency-bound loop that must not call cudaMalloc (which can synchronize the
+ * device).  Such a caller passes only inputs and outputs.
+ *
+ * The FP8 latent and its packed scales, which iq_prepare_q keeps in the
+ * caller's workspace, live instead in one scratch array built into the
+ * library: IQ_STATIC_MAX_TOKENS * 1536 bytes plus the scale words (about
+ * 3.2 MB), held on every GPU that loads the library until the process exits.
+ *
+ * Behaviour:
+ *  - M > IQ_STATIC_MAX_TOKENS returns IQ_ERR_WORKSPACE (the built-in scratch
+ *    is too small) before anything is launched; M == 0 returns IQ_OK.
+ *  - The first call on a device looks up the device address of the scratch
+ *    array (cudaGetSymbolAddress) with that device current; make that first
+ *    call before any stream capture on the device.
+ *  - All calls on a device share the one scratch array, and it keeps what the
+ *    previous call left there.  Nothing in it needs clearing: every byte the
+ *    GEMM kernel reads is written by the quantizer kernel of the same call.
+ *    Calls whose work overlaps on the GPU (for example on two streams without
+ *    ordering between them) race on the scratch and give wrong results;
+ *    order them on one stream or with events.
+ *  - Same arguments, results and errors as iq_prepare_q otherwise; nothing
+ *    is allocated, no allocating library routine is called.
+ * ------------------------------------------------------------------------ */
+
+#define IQ_STATIC_MAX_TOKENS 2048
+
+iq_status iq_prepare_q_static(const void* latent_bf16, int M,
+                              const void* wq_e4m3, const uint8_t* wq_sf,
+                              const int32_t* positions,
+                              uint8_t* q_fp4, uint8_t* q_sf, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
