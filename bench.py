@@ -5,8 +5,9 @@ quantizer on the BF16 latent [4632, 1536], then the fused block-scaled FP8
 GEMM with the RoPE -> Hadamard -> FP4 epilogue, producing packed FP4 Q
 [4632, 4096] and its UE8M0 scales [4632, 256] (the two launches of
 iq_prepare_q).  Inputs are seeded synthetic data resident in HBM before the
-timed region; L2 is flushed (256 MB write) between timed steps, outside the
-CUDA-event intervals.  Also measured in the same run: the quantizer alone on
+timed region; L2 is flushed (256 MB written, then 256 MB read, so no dirty
+lines are left for the timed kernels to write back) between timed steps,
+outside the CUDA-event intervals.  Also measured in the same run: the quantizer alone on
 BF16 [4632, 7168] (GB/s against HBM), the end-to-end call through
 iq_prepare_q with pinned host buffers (copies inside the timed region), and
 the CPU oracle on a bounded sample of the same workload.
@@ -47,7 +48,7 @@ ORACLE_SAMPLE_ROWS = 1024      # rows of the prefill workload per oracle timing
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -91,7 +92,8 @@ def kernel_traffic(kernel_key: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks sampled every 200 ms while the timed region runs."""
+    """nvidia-smi clocks sampled every 20 ms from the start of the chain's timed
+    region to the end of the end-to-end measurement."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -107,7 +109,7 @@ class ClockSampler:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -216,9 +218,13 @@ def run_ours(args):
 
     stream = torch.cuda.current_stream()
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_src = torch.ones(64 << 20, dtype=torch.float32, device=dev)
 
     def flush_l2():
+        # Write 256 MB, then read another 256 MB: the next step finds none of
+        # its data in L2 and no dirty lines of the flush left to write back.
         flush_buf.fill_(rank & 0xFF)
+        flush_src.sum()
 
     # ---------------------------------------------------- the prefill chain
     x, wq, wsf, pos = W.prefill_chain(M_PREFILL)
@@ -240,7 +246,8 @@ def run_ours(args):
         step()
     barrier()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    with ClockSampler(local) as clocks:
+    clocks = ClockSampler(local).__enter__()
+    if True:
         barrier()
         t_wall = time.perf_counter()
         for i in range(args.steps):
@@ -324,6 +331,7 @@ def run_ours(args):
         b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / len(eev)
+    clocks.__exit__(None, None, None)
     e2e = {"value": world * M / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": h_lat.numel() * 2 + h_pos.numel() * 4,
            "d2h_bytes_per_step": h_q.numel() + h_s.numel()}
@@ -345,7 +353,7 @@ def run_ours(args):
                                    "RoPE (positions 0..4631) -> Hadamard-128 -> MXFP4 [4632, 4096] + UE8M0 "
                                    "[4632, 256]",
                        "M": M, "K": K_LATENT, "N": N_Q, "parallelism": f"replicas x{world}",
-                       "l2": "flushed (256 MB write) between timed steps, outside the event intervals"},
+                       "l2": "flushed between timed steps (256 MB write then 256 MB read), outside the event intervals"},
             "roofline": roofline, "quantizer": quantizer, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": 2 * args.steps,
             "clocks": clocks.summary(),
