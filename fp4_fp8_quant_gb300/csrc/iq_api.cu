@@ -23,7 +23,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 struct DeviceInfo {
   bool ready = false;
   iq_status status = IQ_OK;
-  int num_sms = 0;
+  int max_pairs = 0;   // co-resident CTA pairs of the fused GEMM kernel
 };
 
 std::mutex g_setup_mutex;
@@ -35,21 +35,20 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // First call on a device: check the architecture, set kernel attributes and
 // resolve the driver's tensor-map encoder.  Later calls only read the cache.
-iq_status device_setup(int* num_sms) {
+iq_status device_setup(int* max_pairs) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return IQ_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   DeviceInfo& d = g_devices[dev];
   if (!d.ready) {
-    int major = 0, minor = 0, sms = 0;
+    int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
       return IQ_ERR_CUDA;
     }
     if (major != 10 || minor != 3) {
       d.status = IQ_ERR_ARCH;
-    } else if (iq::gemm_setup_device() != cudaSuccess) {
+    } else if (iq::gemm_setup_device(&d.max_pairs) != cudaSuccess || d.max_pairs < 1) {
       d.status = IQ_ERR_CUDA;
     } else {
       d.status = IQ_OK;
@@ -65,22 +64,21 @@ iq_status device_setup(int* num_sms) {
         g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
       }
     }
-    d.num_sms = sms;
     d.ready = true;
   }
-  *num_sms = d.num_sms;
+  *max_pairs = d.max_pairs;
   return d.status;
 }
 
-// 2D uint8 tensor map, inner dimension K bytes, 128-byte swizzled boxes.
+// 2D uint8 tensor map over a row-major [rows][inner] byte matrix.
 bool encode_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                  uint32_t box_rows) {
+                  uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {inner};
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-                                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -99,12 +97,15 @@ iq::RopeTurns make_rope_turns() {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq, const uint8_t* wq_sf,
-                     const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf, float* q_pre, int num_sms,
+                     const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf, float* q_pre, int max_pairs,
                      cudaStream_t stream) {
   static const iq::RopeTurns rope = make_rope_turns();
-  CUtensorMap tm_x, tm_w;
+  // X: this CTA's 128 token rows per K-block; W: one head (128 rows) per
+  // CTA of the pair; Q codes: one head of 128 rows x 64 bytes per store.
+  CUtensorMap tm_x, tm_w, tm_q;
   if (!encode_2d_u8(&tm_x, xq, iq::kLatentDim, static_cast<uint64_t>(M), 128, 128) ||
-      !encode_2d_u8(&tm_w, wq, iq::kLatentDim, iq::kQDim, 128, 256)) {
+      !encode_2d_u8(&tm_w, wq, iq::kLatentDim, iq::kQDim, 128, 256 / iq::gemm_pair_size()) ||
+      !encode_2d_u8(&tm_q, q_fp4, iq::kQDim / 2, static_cast<uint64_t>(M), 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) {
     return IQ_ERR_CUDA;
   }
   iq::GemmArgs a;
@@ -117,10 +118,12 @@ iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq,
   a.M = M;
   a.m_al = (M + 3) / 4 * 4;
   a.num_m_tiles = (M + 127) / 128;
-  a.num_tiles = a.num_m_tiles * (iq::kQDim / 256);
+  a.num_m_pairs = (a.num_m_tiles + iq::gemm_pair_size() - 1) / iq::gemm_pair_size();
+  a.num_pair_tiles = a.num_m_pairs * (iq::kQDim / 256);
   a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   a.rope = rope;
-  return iq::launch_gemm_rope_hadamard_fp4(tm_x, tm_w, a, num_sms, stream) == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
+  return iq::launch_gemm_rope_hadamard_fp4(tm_x, tm_w, tm_q, a, max_pairs, stream) == cudaSuccess ? IQ_OK
+                                                                                                   : IQ_ERR_CUDA;
 }
 
 iq_status check_prepare_args(const void* latent, int M, const void* wq, const uint8_t* wq_sf, const int32_t* pos,
@@ -143,8 +146,8 @@ iq_status prepare_impl(const void* latent, int M, const void* wq, const uint8_t*
   if (!ws) return IQ_ERR_ARG;
   if (!aligned(ws, 256)) return IQ_ERR_ALIGN;
   if (ws_bytes < iq_prepare_q_workspace(M)) return IQ_ERR_WORKSPACE;
-  int num_sms = 0;
-  st = device_setup(&num_sms);
+  int max_pairs = 0;
+  st = device_setup(&max_pairs);
   if (st != IQ_OK) return st;
   uint8_t* xq = static_cast<uint8_t*>(ws);
   int32_t* x_sf = reinterpret_cast<int32_t*>(xq + align_up(static_cast<size_t>(M) * iq::kLatentDim, 256));
@@ -152,7 +155,7 @@ iq_status prepare_impl(const void* latent, int M, const void* wq, const uint8_t*
       cudaSuccess) {
     return IQ_ERR_CUDA;
   }
-  return gemm_stage(xq, x_sf, M, wq, wq_sf, pos, q_fp4, q_sf, q_pre, num_sms, stream);
+  return gemm_stage(xq, x_sf, M, wq, wq_sf, pos, q_fp4, q_sf, q_pre, max_pairs, stream);
 }
 
 }  // namespace
@@ -197,8 +200,8 @@ iq_status iq_fp8_quant_1x128_ue8m0(const void* x_bf16, int M, int K, int ldx, vo
   if (!aligned(x_bf16, 16) || !aligned(y_e4m3, 16) || !aligned(scales, 4) || ldx % 8 != 0 || ldy % 16 != 0) {
     return IQ_ERR_ALIGN;
   }
-  int num_sms = 0;
-  const iq_status st = device_setup(&num_sms);
+  int max_pairs = 0;
+  const iq_status st = device_setup(&max_pairs);
   if (st != IQ_OK) return st;
   return iq::launch_quant_1x128(x_bf16, M, K, ldx, y_e4m3, ldy, scales, stream) == cudaSuccess ? IQ_OK
                                                                                                 : IQ_ERR_CUDA;
@@ -231,10 +234,10 @@ iq_status iq_gemm_rope_hadamard_fp4(const void* xq_e4m3, const int32_t* x_scales
   if (st != IQ_OK || M == 0) return st;
   if (!x_scales) return IQ_ERR_ARG;
   if (!aligned(x_scales, 4)) return IQ_ERR_ALIGN;
-  int num_sms = 0;
-  st = device_setup(&num_sms);
+  int max_pairs = 0;
+  st = device_setup(&max_pairs);
   if (st != IQ_OK) return st;
-  return gemm_stage(xq_e4m3, x_scales, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, q_prequant, num_sms, stream);
+  return gemm_stage(xq_e4m3, x_scales, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, q_prequant, max_pairs, stream);
 }
 
 }  // extern "C"
@@ -280,8 +283,8 @@ extern "C" iq_status iq_prepare_q_static(const void* latent_bf16, int M, const v
   iq_status st = check_prepare_args(latent_bf16, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, nullptr, false);
   if (st != IQ_OK || M == 0) return st;
   if (M > IQ_STATIC_MAX_TOKENS) return IQ_ERR_WORKSPACE;
-  int num_sms = 0;
-  st = device_setup(&num_sms);
+  int max_pairs = 0;
+  st = device_setup(&max_pairs);
   if (st != IQ_OK) return st;
   void* scratch = nullptr;
   st = static_scratch_address(&scratch);
@@ -292,5 +295,5 @@ extern "C" iq_status iq_prepare_q_static(const void* latent_bf16, int M, const v
       cudaSuccess) {
     return IQ_ERR_CUDA;
   }
-  return gemm_stage(xq, x_sf, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, nullptr, num_sms, stream);
+  return gemm_stage(xq, x_sf, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, nullptr, max_pairs, stream);
 }

@@ -9,22 +9,33 @@
 // TokenSpeed PR "perf(deepseek-v4): accelerate indexer Q and packed FP8
 // quantization" (Summary: RoPE, Hadamard and fusedCat FP4 on the indexer Q).
 //
-// Tile: 128 tokens x 256 output features (two heads) per CTA tile, K = 1536 in
-// twelve 128-byte K-blocks.  Persistent CTAs (one per SM) walk the tiles.
-// Warp roles (320 threads):
-//   warp 0      TMA producer: a 4-stage ring of {X tile 16 KB, W tile 32 KB},
-//               128-byte swizzled, plus the per-tile scale factors staged in
-//               shared memory in the layout tcgen05.cp 32x128b expects;
-//   warp 1      TMEM owner and MMA issuer: copies the scale factors into TMEM
-//               and issues tcgen05.mma kind::mxf8f6f4 block_scale (scale vector
-//               1X = one UE8M0 per 32 K) into a 128 x 256 FP32 accumulator;
+// CTA pairs.  The kernel runs in clusters of two CTAs (one per SM) that
+// compute one 256-token x 256-feature (two heads) tile together with the
+// 2-SM form of the MMA (tcgen05 cta_group::2, M = 256): each CTA holds its own
+// 128 token rows of X and the 128 rows of W of one of the two heads, and its
+// tensor memory receives the 128 x 256 FP32 accumulator of its own rows.  On
+// GB300 the 1-SM M = 128 MMA measured 1.3-1.6x slower per SM than this form,
+// which reaches the tensor-core peak.  K = 1536 streams as twelve 128-byte
+// K-blocks.  Each pair takes a contiguous run of tiles in feature-major order,
+// so consecutive tiles mostly share their two heads.
+// Warp roles (320 threads per CTA):
+//   warp 0      TMA producer (both CTAs): a 6-stage ring of {X 16 KB, W 16 KB},
+//               128-byte swizzled; each load signals the leader CTA's barrier.
+//               It also stages the tile's scale factors in shared memory in
+//               the layout tcgen05.cp 32x128b expects;
+//   warp 1      TMEM owner (both CTAs) and, in the leader CTA, MMA issuer: it
+//               copies the scale factors into both CTAs' tensor memories and
+//               issues tcgen05.mma kind::mxf8f6f4 block_scale (scale vector 1X =
+//               one UE8M0 per 32 K) for the pair;
 //   warps 2..9  epilogue: each thread owns one (token, head) pair = one TMEM
 //               lane x 128 columns.  It drains its 128 values to registers,
-//               releases the accumulator at once so the next tile's MMAs can
-//               start, then does RoPE, the in-register 128-point fast
-//               Walsh-Hadamard transform, the FP4 block quantization and the
-//               stores.  The FP32 pre-quant Q never touches memory unless the
-//               debug output is requested.
+//               releases the accumulator at once, then does RoPE, the 128-point
+//               fast Walsh-Hadamard transform and the FP4 block quantization in
+//               packed FP32x2 arithmetic (scalar FP32 add/mul/fma next to the
+//               MMAs slow the tensor pipe on GB300; the packed forms do not),
+//               and stages the FP4 codes in shared memory, from where two bulk
+//               tensor stores per tile write them.  The FP32 pre-quant Q never
+//               touches memory unless the debug output is requested.
 //
 // Scale factors.  The activation scales are per 1x128 block and the weight
 // scales per 128x128 block, but the MMA applies one scale per 32 K: every
@@ -34,9 +45,11 @@
 // powers of two.
 //
 // Every mbarrier wait is bounded (GemmArgs::timeout_ns); a wait that gives up
-// records its kind in the device status word, raises a CTA-wide abort flag so
-// the other roles leave their loops, and the teardown waits (bounded) for the
-// CTA's own TMA loads and tcgen05 operations before TMEM is freed.
+// records its kind in the device status word and raises a CTA abort flag so
+// the other roles leave their loops; the epilogue warps take their exit
+// decision together.  The teardown waits (bounded) until the pair's MMAs have
+// released every stage this CTA loaded and completed, and both CTAs meet at a
+// cluster barrier before tensor memory is freed.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -52,13 +65,15 @@ __device__ uint32_t g_iq_status;
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128;                          // token rows per CTA (256 per pair)
+constexpr int BN = 256;                          // output features per tile (two heads)
 constexpr int BK = 128;
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK;                 // 16 KB
-constexpr int kBBytes = BN * BK;                 // 32 KB
-constexpr int kStageTx = kABytes + kBBytes;
+constexpr int kPair = 2;
+constexpr uint16_t kPairMask = 0x3;
+constexpr int kStages = 6;
+constexpr int kABytes = BM * BK;                 // 16 KB: this CTA's token rows
+constexpr int kBBytes = (BN / kPair) * BK;       // 16 KB: this CTA's head of W
+constexpr int kPairStageTx = kPair * (kABytes + kBBytes);   // bytes landing per stage, both CTAs
 constexpr int kNumEpiWarps = 8;
 constexpr int kThreads = (2 + kNumEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
@@ -73,7 +88,9 @@ constexpr int kSfaWords = kScaleGroups * 128;    // per buffer
 constexpr int kSfbWords = kScaleGroups * 256;
 constexpr int kOffSfa = kOffB + kStages * kBBytes;
 constexpr int kOffSfb = kOffSfa + 2 * kSfaWords * 4;
-constexpr int kOffBar = kOffSfb + 2 * kSfbWords * 4;
+constexpr int kOffOut = kOffSfb + 2 * kSfbWords * 4;   // FP4 code staging: [2 heads][128 rows][64 B]
+constexpr int kOutHeadBytes = BM * 64;
+constexpr int kOffBar = kOffOut + 2 * kOutHeadBytes;
 constexpr int kNumBars = 2 * kStages + 4 + 3;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
@@ -95,33 +112,60 @@ __device__ __forceinline__ int fp4_scale_exponent(float a) {
   return E - 2 + ((bits & 0x7FFFFFu) > 0x400000u ? 1 : 0);
 }
 
-// RoPE, Hadamard, FP4 for one (token, head): v holds the 128 FP32 GEMM outputs.
-__device__ __forceinline__ void epilogue_row(float (&v)[128], int row, int head, const GemmArgs& args) {
+// RoPE, Hadamard, FP4 for one (token, head).  p[j] holds dims (2j, 2j+1) of
+// the 128 FP32 GEMM outputs as one packed pair.  The FP4 codes go to
+// `stage_row`, this row's 64 bytes of the shared staging tile, stored with the
+// 64-byte swizzle of the bulk tensor store (16-byte chunk c of row r at chunk
+// c ^ ((r >> 1) & 3)): a warp's 16-byte writes then fall on distinct banks.
+__device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int head, int pos, const GemmArgs& args,
+                                             uint8_t* stage_row, int swz) {
   // NeoX RoPE on dims 0..63: pairs (i, i+32), angle = pos * 10000^(-i/32).
-  // The angle is reduced in turns with a two-float product so that it stays
-  // accurate for large positions; the reduced angle lies in [-pi, pi].
-  const float p = static_cast<float>(args.pos[row]);
+  // The angle is reduced in turns with a two-float product (head and tail of
+  // the frequency, exact FMA residue) so that it stays accurate for large
+  // positions; the reduced angle lies in [-pi, pi].  Frequencies i and i+1 go
+  // through the packed lanes together; rounding to an integer uses the
+  // 1.5 * 2^23 shift, exact for |turns| < 2^22.
+  const float pf = static_cast<float>(pos);
+  const uint64_t pp = f2_pack(pf, pf);
+  const uint64_t shift = f2_pack(12582912.0f, 12582912.0f);
+  const uint64_t two_pi = f2_pack(kTwoPi, kTwoPi);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float th = p * args.rope.hi[i];
-    float tl = fmaf(p, args.rope.hi[i], -th);
-    tl = fmaf(p, args.rope.lo[i], tl);
-    const float fr = (th - rintf(th)) + tl;
-    float s, c;
-    __sincosf(fr * kTwoPi, &s, &c);
-    const float x1 = v[i], x2 = v[i + 32];
-    v[i] = x1 * c - x2 * s;
-    v[i + 32] = x2 * c + x1 * s;
+  for (int i = 0; i < 32; i += 2) {
+    const uint64_t hi = f2_pack(args.rope.hi[i], args.rope.hi[i + 1]);
+    const uint64_t lo = f2_pack(args.rope.lo[i], args.rope.lo[i + 1]);
+    const uint64_t th = f2_mul(pp, hi);
+    uint64_t tl = f2_fma(pp, hi, f2_neg(th));
+    tl = f2_fma(pp, lo, tl);
+    const uint64_t rn = f2_sub(f2_add(th, shift), shift);
+    const uint64_t ang = f2_mul(f2_add(f2_sub(th, rn), tl), two_pi);
+    float a0, a1, s0, c0, s1, c1;
+    f2_unpack(ang, a0, a1);
+    __sincosf(a0, &s0, &c0);
+    __sincosf(a1, &s1, &c1);
+    const uint64_t c = f2_pack(c0, c1);
+    const uint64_t s = f2_pack(s0, s1);
+    const uint64_t x1 = p[i >> 1], x2 = p[(i >> 1) + 16];
+    p[i >> 1] = f2_fma(x1, c, f2_mul(x2, f2_neg(s)));        // x1 c - x2 s
+    p[(i >> 1) + 16] = f2_fma(x2, c, f2_mul(x1, s));         // x2 c + x1 s
   }
-  // Fast Walsh-Hadamard transform in Sylvester order (unscaled).
+  // Fast Walsh-Hadamard transform in Sylvester order (unscaled).  The stage
+  // pairing dims that differ in bit 0 works inside each packed pair:
+  // (a, b) -> (a + b, a - b) = (a, b) * (1, -1) + (b, a).
+  const uint64_t one_neg = f2_pack(1.0f, -1.0f);
 #pragma unroll
-  for (int h = 1; h < 128; h <<= 1) {
+  for (int j = 0; j < 64; ++j) {
+    float a, b;
+    f2_unpack(p[j], a, b);
+    p[j] = f2_fma(p[j], one_neg, f2_pack(b, a));
+  }
 #pragma unroll
-    for (int i = 0; i < 128; ++i) {
-      if ((i & h) == 0) {
-        const float a = v[i], b = v[i + h];
-        v[i] = a + b;
-        v[i + h] = a - b;
+  for (int h = 1; h < 64; h <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      if ((j & h) == 0) {
+        const uint64_t a = p[j], b = p[j + h];
+        p[j] = f2_add(a, b);
+        p[j + h] = f2_sub(a, b);
       }
     }
   }
@@ -133,104 +177,139 @@ __device__ __forceinline__ void epilogue_row(float (&v)[128], int row, int head,
   for (int b = 0; b < 4; ++b) {
     float amax = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[32 * b + j]));
+    for (int j = 0; j < 16; ++j) {
+      float x0, x1;
+      f2_unpack(p[16 * b + j], x0, x1);
+      amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+    }
     const int e = fp4_scale_exponent(amax * kInvSqrt128);
     const float k = __uint_as_float(static_cast<uint32_t>(127 - e) << 23) * kInvSqrt128;
+    const uint64_t kk = f2_pack(k, k);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       float q[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) q[j] = v[32 * b + 8 * t + j] * k;
+      for (int j = 0; j < 4; ++j) f2_unpack(f2_mul(p[16 * b + 4 * t + j], kk), q[2 * j], q[2 * j + 1]);
       codes[4 * b + t] = cvt_e2m1x8(q);
     }
     sfw |= static_cast<uint32_t>(e + 127) << (8 * b);
   }
-  uint4* dst = reinterpret_cast<uint4*>(args.q_fp4 + static_cast<long long>(row) * (kQDim / 2) + head * 64);
 #pragma unroll
   for (int t = 0; t < 4; ++t)
-    dst[t] = make_uint4(codes[4 * t], codes[4 * t + 1], codes[4 * t + 2], codes[4 * t + 3]);
+    *reinterpret_cast<uint4*>(stage_row + ((t ^ swz) << 4)) =
+        make_uint4(codes[4 * t], codes[4 * t + 1], codes[4 * t + 2], codes[4 * t + 3]);
   *reinterpret_cast<uint32_t*>(args.q_sf + static_cast<long long>(row) * (kQDim / 32) + head * 4) = sfw;
   if (args.q_pre != nullptr) {
+    const uint64_t c2 = f2_pack(kInvSqrt128, kInvSqrt128);
     float4* pre = reinterpret_cast<float4*>(args.q_pre + static_cast<long long>(row) * kQDim + head * kHeadDim);
 #pragma unroll
-    for (int t = 0; t < 32; ++t)
-      pre[t] = make_float4(v[4 * t] * kInvSqrt128, v[4 * t + 1] * kInvSqrt128, v[4 * t + 2] * kInvSqrt128,
-                           v[4 * t + 3] * kInvSqrt128);
+    for (int t = 0; t < 32; ++t) {
+      float z0, z1, z2, z3;
+      f2_unpack(f2_mul(p[2 * t], c2), z0, z1);
+      f2_unpack(f2_mul(p[2 * t + 1], c2), z2, z3);
+      pre[t] = make_float4(z0, z1, z2, z3);
+    }
   }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_rope_hadamard_fp4_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                                  const __grid_constant__ GemmArgs args) {
+                                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem + kOffA;
   uint8_t* sB = smem + kOffB;
   uint32_t* sSfa = reinterpret_cast<uint32_t*>(smem + kOffSfa);
   uint32_t* sSfb = reinterpret_cast<uint32_t*>(smem + kOffSfb);
+  uint8_t* sOut = smem + kOffOut;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* sf_full = bars + 2 * kStages;
-  uint64_t* sf_empty = sf_full + 2;
-  uint64_t* tmem_full = sf_empty + 2;
-  uint64_t* tmem_empty = tmem_full + 1;
-  uint64_t* final_bar = tmem_empty + 1;
+  uint64_t* full = bars;                       // leader: both CTAs' loads of a stage landed
+  uint64_t* empty = bars + kStages;            // both: the pair's MMAs released a stage
+  uint64_t* sf_full = bars + 2 * kStages;      // leader: both CTAs staged a tile's scales
+  uint64_t* sf_empty = sf_full + 2;            // both: the scale copies completed
+  uint64_t* tmem_full = sf_empty + 2;          // both: the tile's accumulator is complete
+  uint64_t* tmem_empty = tmem_full + 1;        // leader: both CTAs drained the accumulator
+  uint64_t* final_bar = tmem_empty + 1;        // both: every pair MMA has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t timeout = args.timeout_ns;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
 
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_q);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sf_full[b], 1);
+      mbar_init(&sf_full[b], kPair);
       mbar_init(&sf_empty[b], 1);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, kNumEpiWarps);
+    mbar_init(tmem_empty, kPair * kNumEpiWarps);
     mbar_init(final_bar, 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
   }
+  // Barriers and tensor memory must be ready in both CTAs before either
+  // issues anything that touches the other.
   tc_fence_before_sync();
-  __syncthreads();
+  cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  const int num_m_tiles = args.num_m_tiles;
+  // Leader-CTA addresses of the barriers that collect the pair's work.
+  const uint32_t full_leader0 = mapa_shared(smem_u32(&full[0]), 0);
+  const uint32_t sf_full_leader0 = mapa_shared(smem_u32(&sf_full[0]), 0);
+  const uint32_t tmem_empty_leader = mapa_shared(smem_u32(tmem_empty), 0);
+
+  // Pair tile pt: token rows [256 * (pt % num_m_pairs), +256) split by CTA
+  // rank, features [256 * (pt / num_m_pairs), +256).  Each pair takes a
+  // contiguous run of tiles, so consecutive tiles mostly share the same two
+  // heads: their W tiles stay hot in L2 and their weight scales are staged
+  // and copied into tensor memory only when the heads change.
+  const int num_pairs = static_cast<int>(cluster_count_x());
+  const int tiles_per_pair = (args.num_pair_tiles + num_pairs - 1) / num_pairs;
+  const int first_pt = static_cast<int>(cluster_id_x()) * tiles_per_pair;
+  const int end_pt = min(first_pt + tiles_per_pair, args.num_pair_tiles);
+  const int num_m_pairs = args.num_m_pairs;
+  auto tile_m0 = [&](int pt) { return ((pt % num_m_pairs) * kPair + static_cast<int>(rank)) * BM; };
+  auto tile_n = [&](int pt) { return pt / num_m_pairs; };
+  auto new_heads = [&](int pt) { return pt == first_pt || tile_n(pt - 1) != tile_n(pt); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, issued_phase = 0;   // per stage: a load was issued / its phase
     int local = 0;
-    for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++local) {
+    for (int pt = first_pt; pt < end_pt; ++pt, ++local) {
       // Every exit decision is made warp-uniform: the lanes must stay
       // converged for the shuffles below.
       if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
-      const int m0 = (tile % num_m_tiles) * BM;
-      const int n_tile = tile / num_m_tiles;
+      const int m0 = tile_m0(pt);
+      const int n_tile = tile_n(pt);
       const int buf = local & 1;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_empty[buf], ((local >> 1) & 1) ^ 1, timeout))) {
         if (lane == 0) fail(abort_flag, kStatusProducerWait);
         break;
       }
       // Scale factors in the tcgen05.cp 32x128b layout: word [r * 4 + c] of a
-      // 128-row tile holds row c * 32 + r.
+      // 128-row tile holds row c * 32 + r.  SFA: this CTA's 128 token rows;
+      // SFB: both heads of the tile (all 256 rows), staged only when the heads
+      // differ from the previous tile's (the MMA issuer copies it only then).
       uint32_t* sfa = sSfa + buf * kSfaWords;
       uint32_t* sfb = sSfb + buf * kSfbWords;
+      const bool stage_sfb = new_heads(pt);
 #pragma unroll
       for (int g = 0; g < kScaleGroups; ++g) {
 #pragma unroll
@@ -239,30 +318,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           sfa[g * 128 + lane * 4 + c] =
               m < args.m_al ? static_cast<uint32_t>(__ldg(args.x_sf + static_cast<long long>(g) * args.m_al + m)) : 0u;
         }
+        if (stage_sfb) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint8_t* ws = args.w_sf + (n_tile * 2 + half) * kNumKBlocks + 4 * g;
-          const uint32_t word = static_cast<uint32_t>(__ldg(ws)) | (static_cast<uint32_t>(__ldg(ws + 1)) << 8) |
-                                (static_cast<uint32_t>(__ldg(ws + 2)) << 16) |
-                                (static_cast<uint32_t>(__ldg(ws + 3)) << 24);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) sfb[g * 256 + half * 128 + lane * 4 + c] = word;
+          for (int half = 0; half < 2; ++half) {
+            const uint8_t* ws = args.w_sf + (n_tile * 2 + half) * kNumKBlocks + 4 * g;
+            const uint32_t word = static_cast<uint32_t>(__ldg(ws)) | (static_cast<uint32_t>(__ldg(ws + 1)) << 8) |
+                                  (static_cast<uint32_t>(__ldg(ws + 2)) << 16) |
+                                  (static_cast<uint32_t>(__ldg(ws + 3)) << 24);
+            *reinterpret_cast<uint4*>(sfb + g * 256 + half * 128 + lane * 4) = make_uint4(word, word, word, word);
+          }
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
       bool ok = true;
       if (lane == 0) {
-        mbar_arrive(&sf_full[buf]);
+        mbar_arrive_cluster(sf_full_leader0 + 8u * static_cast<uint32_t>(buf));
         for (int kb = 0; kb < kNumKBlocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, timeout)) {
             fail(abort_flag, kStatusProducerWait);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], kStageTx);
-          tma_load_2d(sA + stage * kABytes, &tm_x, &full[stage], kb * BK, m0);
-          tma_load_2d(sB + stage * kBBytes, &tm_w, &full[stage], kb * BK, n_tile * BN);
+          if (leader) mbar_arrive_expect_tx(&full[stage], kPairStageTx);
+          const uint32_t bar = full_leader0 + 8u * stage;
+          tma_load_2d_pair(sA + stage * kABytes, &tm_x, bar, kb * BK, m0);
+          tma_load_2d_pair(sB + stage * kBBytes, &tm_w, bar, kb * BK,
+                           n_tile * BN + static_cast<int>(rank) * (BN / kPair));
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -274,67 +356,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
     }
-    // Teardown: the last load issued into each stage must have landed before
-    // the shared memory can be released.
+    // Teardown: this CTA's loads signal the leader's barriers, so their
+    // landing is observed through the stage's release by the pair's MMAs,
+    // which consumed them.
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s) {
         if ((issued_mask >> s) & 1u) {
-          if (!mbar_wait(&full[s], (issued_phase >> s) & 1u, timeout)) fail(abort_flag, kStatusTeardownWait);
+          if (!mbar_wait(&empty[s], (issued_phase >> s) & 1u, timeout)) fail(abort_flag, kStatusTeardownWait);
         }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
+    // ----------------------------------------------------- MMA issuer (leader)
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      int local = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < args.num_tiles && ok; tile += gridDim.x, ++local) {
-        if (*abort_flag) break;
-        const int buf = local & 1;
-        if (!mbar_wait(&sf_full[buf], (local >> 1) & 1, timeout) ||
-            !mbar_wait(tmem_empty, (local & 1) ^ 1, timeout)) {
-          fail(abort_flag, kStatusMmaWait);
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t* sfa = sSfa + buf * kSfaWords;
-        const uint32_t* sfb = sSfb + buf * kSfbWords;
-#pragma unroll
-        for (int g = 0; g < kScaleGroups; ++g) {
-          tc_cp_32x128b_warpx4(tmem + kSfaCol + 8 * g, smem_desc_sf(smem_u32(sfa + g * 128)));
-          tc_cp_32x128b_warpx4(tmem + kSfbCol + 8 * g, smem_desc_sf(smem_u32(sfb + g * 256)));
-          tc_cp_32x128b_warpx4(tmem + kSfbCol + 8 * g + 4, smem_desc_sf(smem_u32(sfb + g * 256 + 128)));
-        }
-        tc_commit(&sf_empty[buf]);
-        for (int kb = 0; kb < kNumKBlocks; ++kb) {
-          if (*abort_flag || !mbar_wait(&full[stage], phase, timeout)) {
+      if (leader) {
+        uint32_t stage = 0, phase = 0;
+        int local = 0;
+        bool ok = true;
+        const uint64_t adesc0 = smem_desc_sw128(smem_u32(sA));
+        const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sB));
+        const uint32_t idesc0 = idesc_mxf8_e4m3(kPair * BM, BN, 0, 0);
+        for (int pt = first_pt; pt < end_pt && ok; ++pt, ++local) {
+          if (*abort_flag) break;
+          const int buf = local & 1;
+          if (!mbar_wait(&sf_full[buf], (local >> 1) & 1, timeout) ||
+              !mbar_wait(tmem_empty, (local & 1) ^ 1, timeout)) {
             fail(abort_flag, kStatusMmaWait);
-            ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint64_t adesc = smem_desc_sw128(smem_u32(sA + stage * kABytes));
-          const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + stage * kBBytes));
-          const uint32_t idesc = idesc_mxf8_e4m3(BM, BN, kb & 3, kb & 3);
-          const uint32_t sfa_t = tmem + kSfaCol + 8 * (kb >> 2);
-          const uint32_t sfb_t = tmem + kSfbCol + 8 * (kb >> 2);
+          const uint32_t* sfa = sSfa + buf * kSfaWords;
+          const uint32_t* sfb = sSfb + buf * kSfbWords;
+          const bool copy_sfb = new_heads(pt);
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k) {
-            // advance 32 bytes along K inside the 128-byte swizzle atom
-            tc_mma_mxf8(tmem + kAccCol, adesc + 2 * k, bdesc + 2 * k, idesc, sfa_t, sfb_t, (kb | k) != 0);
+          for (int g = 0; g < kScaleGroups; ++g) {
+            tc_cp_32x128b_warpx4_pair(tmem + kSfaCol + 8 * g, smem_desc_sf(smem_u32(sfa + g * 128)));
+            if (copy_sfb) {
+              tc_cp_32x128b_warpx4_pair(tmem + kSfbCol + 8 * g, smem_desc_sf(smem_u32(sfb + g * 256)));
+              tc_cp_32x128b_warpx4_pair(tmem + kSfbCol + 8 * g + 4, smem_desc_sf(smem_u32(sfb + g * 256 + 128)));
+            }
           }
-          tc_commit(&empty[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
+          tc_commit_pair(&sf_empty[buf], kPairMask);
+          // The K loop does little between MMAs.  TMA data needs no tcgen05
+          // fence: the barrier's transaction completion orders it.
+          for (int kb = 0; kb < kNumKBlocks; ++kb) {
+            if (!mbar_wait(&full[stage], phase, timeout)) {
+              fail(abort_flag, kStatusMmaWait);
+              ok = false;
+              break;
+            }
+            const uint64_t adesc = adesc0 + static_cast<uint64_t>(stage * (kABytes >> 4));
+            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * (kBBytes >> 4));
+            const uint32_t sfid = static_cast<uint32_t>(kb & 3);
+            const uint32_t idesc = idesc0 | (sfid << 4) | (sfid << 29);
+            const uint32_t sf_off = 8u * static_cast<uint32_t>(kb >> 2);
+#pragma unroll
+            for (int k = 0; k < BK / 32; ++k) {
+              // advance 32 bytes along K inside the 128-byte swizzle atom
+              tc_mma_mxf8_pair(tmem + kAccCol, adesc + 2 * k, bdesc + 2 * k, idesc, tmem + kSfaCol + sf_off,
+                               tmem + kSfbCol + sf_off, (kb | k) != 0);
+            }
+            tc_commit_pair(&empty[stage], kPairMask);   // frees the stage in both CTAs
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
+          if (ok) tc_commit_pair(tmem_full, kPairMask);
         }
-        if (ok) tc_commit(tmem_full);
+        tc_commit_pair(final_bar, kPairMask);
       }
-      // Teardown: every tcgen05 operation of this thread has completed.
-      tc_commit(final_bar);
+      // Teardown (both CTAs): every pair MMA writing this CTA's tensor memory
+      // or reading its shared memory has completed.
       if (!mbar_wait(final_bar, 0, timeout)) fail(abort_flag, kStatusTeardownWait);
     }
     __syncwarp();
@@ -342,14 +436,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;            // the TMEM lane group this warp may read
     const int half = (warp - 2) >> 2;     // which head of the tile
+    const int trow = quad * 32 + lane;    // row within the CTA's 128-row tile
+    uint8_t* stage_row = sOut + half * kOutHeadBytes + trow * 64;
+    const int swz = (trow >> 1) & 3;
+    const bool store_issuer = warp == 2 && lane == 0;
     int local = 0;
-    for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++local) {
-      // Warp-uniform exit decisions: tcgen05.ld below is .sync.aligned.
-      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(tmem_full, local & 1, timeout))) {
-        if (lane == 0) fail(abort_flag, kStatusEpilogueWait);
-        break;
-      }
+    for (int pt = first_pt; pt < end_pt; ++pt, ++local) {
+      const int row = tile_m0(pt) + trow;
+      const int head = tile_n(pt) * 2 + half;
+      const int pos = row < args.M ? __ldg(args.pos + row) : 0;   // in flight during the wait
+      // The previous tile's bulk stores must have read the staging tile
+      // before anyone overwrites it.
+      if (store_issuer) tma_store_wait_read();
+      const bool got = mbar_wait(tmem_full, local & 1, timeout);
+      if (!got) fail(abort_flag, kStatusEpilogueWait);
+      // One decision for all epilogue warps (they meet at a named barrier
+      // below); this barrier also tells them the staging tile is free.
+      if (!named_barrier_and(1, kNumEpiWarps * 32, got && *abort_flag == 0u)) break;
       tc_fence_after_sync();
       float v[128];
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kAccCol + half * 128;
@@ -363,35 +466,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait(v + 96);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_empty);
-      const int row = (tile % num_m_tiles) * BM + quad * 32 + lane;
-      const int head = (tile / num_m_tiles) * 2 + half;
-      if (row < args.M) epilogue_row(v, row, head, args);
+      // The accumulator values are in registers (tcgen05.wait::ld above), so
+      // the leader may overwrite it: a CTA-scope arrive suffices and does not
+      // wait for earlier global stores to reach L2.
+      if (lane == 0) mbar_arrive_remote(tmem_empty_leader);
+      uint64_t p[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) p[j] = f2_pack(v[2 * j], v[2 * j + 1]);
+      if (row < args.M) epilogue_row(p, row, head, pos, args, stage_row, swz);
+      fence_proxy_async_smem();
+      named_barrier_sync(1, kNumEpiWarps * 32);
+      if (store_issuer) {
+        // Rows past M are clipped by the bulk store.
+        tma_store_2d(&tm_q, sOut, tile_n(pt) * 2 * 64, tile_m0(pt));
+        tma_store_2d(&tm_q, sOut + kOutHeadBytes, (tile_n(pt) * 2 + 1) * 64, tile_m0(pt));
+        tma_store_commit();
+      }
     }
+    if (store_issuer) tma_store_wait_all();
   }
 
+  // Neither CTA leaves (or frees tensor memory) while the pair may still use
+  // its shared memory, barriers or tensor memory.
   tc_fence_before_sync();
-  __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
+}
+
+cudaLaunchConfig_t pair_config(int pairs, cudaLaunchAttribute* attr, cudaStream_t stream) {
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pairs * kPair, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
 }
 
 }  // namespace
 
 int gemm_smem_bytes() { return kSmemBytes; }
 
-cudaError_t gemm_setup_device() {
-  return cudaFuncSetAttribute(gemm_rope_hadamard_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemBytes);
+int gemm_pair_size() { return kPair; }
+
+cudaError_t gemm_setup_device(int* max_pairs) {
+  cudaError_t err = cudaFuncSetAttribute(gemm_rope_hadamard_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+  if (err != cudaSuccess) return err;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pair_config(1, attr, nullptr);
+  return cudaOccupancyMaxActiveClusters(max_pairs, gemm_rope_hadamard_fp4_kernel, &cfg);
 }
 
-cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const GemmArgs& args,
-                                          int num_sms, cudaStream_t stream) {
-  const int grid = args.num_tiles < num_sms ? args.num_tiles : num_sms;
-  gemm_rope_hadamard_fp4_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_x, tm_w, args);
-  return cudaGetLastError();
+cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
+                                          const GemmArgs& args, int max_pairs, cudaStream_t stream) {
+  const int pairs = args.num_pair_tiles < max_pairs ? args.num_pair_tiles : max_pairs;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pair_config(pairs, attr, stream);
+  return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel, tm_x, tm_w, tm_q, args);
 }
 
 cudaError_t read_device_status(uint32_t* flags, bool reset) {

@@ -37,7 +37,8 @@ struct GemmArgs {
   int M;
   int m_al;
   int num_m_tiles;
-  int num_tiles;
+  int num_m_pairs;       // ceil(num_m_tiles / 2): 256-token row blocks of a CTA pair
+  int num_pair_tiles;    // num_m_pairs * 32 feature tiles of 256
   unsigned long long timeout_ns;
   RopeTurns rope;
 };
@@ -53,12 +54,14 @@ enum : uint32_t {
 cudaError_t launch_quant_1x128(const void* x, int M, int K, long long ldx, void* y, long long ldy, int32_t* sf,
                                cudaStream_t stream);
 
-// Kernel attribute set-up of the fused GEMM on the current device.
-cudaError_t gemm_setup_device();
+// Kernel attribute set-up of the fused GEMM on the current device; returns
+// how many of its CTA pairs fit on the device at once.
+cudaError_t gemm_setup_device(int* max_pairs);
 int gemm_smem_bytes();
+int gemm_pair_size();
 
-cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const GemmArgs& args,
-                                          int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
+                                          const GemmArgs& args, int max_pairs, cudaStream_t stream);
 
 // Device status word access (synchronous).
 cudaError_t read_device_status(uint32_t* flags, bool reset);
