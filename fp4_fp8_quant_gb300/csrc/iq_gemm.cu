@@ -267,6 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // Launched with programmatic stream serialization: everything above
+  // overlapped the preceding kernel; nothing below runs before it completed
+  // (no global memory is read or written before this point).
+  grid_dependency_wait();
 
   // Leader-CTA addresses of the barriers that collect the pair's work.
   const uint32_t full_leader0 = mapa_shared(smem_u32(&full[0]), 0);
@@ -291,6 +295,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, issued_phase = 0;   // per stage: a load was issued / its phase
+    // The next tile's scale words are fetched into registers while the
+    // current tile's K-blocks stream, so no global-load latency sits at a
+    // tile boundary.  ra: this lane's 4 rows x 3 groups of activation-scale
+    // words; rb: the two heads' weight-scale words per group.
+    uint32_t ra[kScaleGroups][4], rb[kScaleGroups][2];
+    auto fetch_scales = [&](int pt) {
+      if (pt >= end_pt) return;
+      const int m0 = tile_m0(pt);
+      const int n_tile = tile_n(pt);
+#pragma unroll
+      for (int g = 0; g < kScaleGroups; ++g) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int m = m0 + c * 32 + lane;
+          ra[g][c] =
+              m < args.m_al ? static_cast<uint32_t>(__ldg(args.x_sf + static_cast<long long>(g) * args.m_al + m)) : 0u;
+        }
+        if (new_heads(pt)) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint8_t* ws = args.w_sf + (n_tile * 2 + half) * kNumKBlocks + 4 * g;
+            rb[g][half] = static_cast<uint32_t>(__ldg(ws)) | (static_cast<uint32_t>(__ldg(ws + 1)) << 8) |
+                          (static_cast<uint32_t>(__ldg(ws + 2)) << 16) | (static_cast<uint32_t>(__ldg(ws + 3)) << 24);
+          }
+        }
+      }
+    };
+    fetch_scales(first_pt);
     int local = 0;
     for (int pt = first_pt; pt < end_pt; ++pt, ++local) {
       // Every exit decision is made warp-uniform: the lanes must stay
@@ -312,25 +344,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool stage_sfb = new_heads(pt);
 #pragma unroll
       for (int g = 0; g < kScaleGroups; ++g) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int m = m0 + c * 32 + lane;
-          sfa[g * 128 + lane * 4 + c] =
-              m < args.m_al ? static_cast<uint32_t>(__ldg(args.x_sf + static_cast<long long>(g) * args.m_al + m)) : 0u;
-        }
+        *reinterpret_cast<uint4*>(sfa + g * 128 + lane * 4) = make_uint4(ra[g][0], ra[g][1], ra[g][2], ra[g][3]);
         if (stage_sfb) {
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint8_t* ws = args.w_sf + (n_tile * 2 + half) * kNumKBlocks + 4 * g;
-            const uint32_t word = static_cast<uint32_t>(__ldg(ws)) | (static_cast<uint32_t>(__ldg(ws + 1)) << 8) |
-                                  (static_cast<uint32_t>(__ldg(ws + 2)) << 16) |
-                                  (static_cast<uint32_t>(__ldg(ws + 3)) << 24);
-            *reinterpret_cast<uint4*>(sfb + g * 256 + half * 128 + lane * 4) = make_uint4(word, word, word, word);
-          }
+          for (int half = 0; half < 2; ++half)
+            *reinterpret_cast<uint4*>(sfb + g * 256 + half * 128 + lane * 4) =
+                make_uint4(rb[g][half], rb[g][half], rb[g][half], rb[g][half]);
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
+      fetch_scales(pt + 1);
       bool ok = true;
       if (lane == 0) {
         mbar_arrive_cluster(sf_full_leader0 + 8u * static_cast<uint32_t>(buf));
@@ -496,18 +520,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Cluster of two, plus programmatic stream serialization: the kernel may be
+// scheduled while the preceding kernel of the stream (the quantizer) runs;
+// it waits for that kernel's completion (griddepcontrol.wait) before any
+// global memory access.
 cudaLaunchConfig_t pair_config(int pairs, cudaLaunchAttribute* attr, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kPair;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pairs * kPair, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
@@ -521,7 +551,7 @@ cudaError_t gemm_setup_device(int* max_pairs) {
   cudaError_t err = cudaFuncSetAttribute(gemm_rope_hadamard_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
   if (err != cudaSuccess) return err;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pair_config(1, attr, nullptr);
   return cudaOccupancyMaxActiveClusters(max_pairs, gemm_rope_hadamard_fp4_kernel, &cfg);
 }
@@ -529,7 +559,7 @@ cudaError_t gemm_setup_device(int* max_pairs) {
 cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
                                           const GemmArgs& args, int max_pairs, cudaStream_t stream) {
   const int pairs = args.num_pair_tiles < max_pairs ? args.num_pair_tiles : max_pairs;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pair_config(pairs, attr, stream);
   return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel, tm_x, tm_w, tm_q, args);
 }

@@ -113,6 +113,18 @@ __device__ __forceinline__ void tma_store_wait_read() {
 // Waits until every committed bulk store of this thread has completed.
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// ----------------------------------------- programmatic dependent launch
+
+// Blocks until the grids this grid depends on (the preceding kernel of the
+// stream, when launched with programmatic stream serialization) have
+// completed and their memory is visible; returns at once otherwise.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the dependent grid of the stream be scheduled before this one ends.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------- barriers / cluster
 
 // Named barrier over `count` threads (a multiple of 32).

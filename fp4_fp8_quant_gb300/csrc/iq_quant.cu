@@ -69,6 +69,9 @@ __global__ void __launch_bounds__(kThreads) quant_1x128_kernel(const uint16_t* _
                                                                long long ldx, uint8_t* __restrict__ y,
                                                                long long ldy, int32_t* __restrict__ sf, int m_al,
                                                                int groups) {
+  // The fused GEMM that usually follows may be scheduled now; it waits for
+  // this grid's completion before reading anything.
+  grid_launch_dependents();
   const long long unit = (static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (unit >= static_cast<long long>(m_al) * groups) return;
