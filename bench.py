@@ -1,16 +1,18 @@
 """Benchmark of the indexer-Q preparation path on GB300.
 
-One step = one pass of the whole hot path over one batch: the FP8 1x128
-quantizer on the BF16 latent [4632, 1536], then the fused block-scaled FP8
-GEMM with the RoPE -> Hadamard -> FP4 epilogue, producing packed FP4 Q
-[4632, 4096] and its UE8M0 scales [4632, 256] (the two launches of
-iq_prepare_q).  Inputs are seeded synthetic data resident in HBM before the
-timed region; L2 is flushed (256 MB written, then 256 MB read, so no dirty
+One step = one pass of the whole hot path over one batch: one iq_prepare_q
+call on the BF16 latent [4632, 1536] -- the FP8 1x128 quantizer, then the
+fused block-scaled FP8 GEMM with the RoPE -> Hadamard -> FP4 epilogue
+(launched as the quantizer's programmatic dependent), producing packed FP4 Q
+[4632, 4096] and its UE8M0 scales [4632, 256].  Inputs are seeded
+synthetic data resident in HBM before the timed region; L2 is flushed (256 MB written, then 256 MB read, so no dirty
 lines are left for the timed kernels to write back) between timed steps,
 outside the CUDA-event intervals.  Also measured in the same run: the quantizer alone on
-BF16 [4632, 7168] (GB/s against HBM), the end-to-end call through
-iq_prepare_q with pinned host buffers (copies inside the timed region), and
-the CPU oracle on a bounded sample of the same workload.
+BF16 [4632, 7168] (GB/s against HBM), the GEMM's own launch time (for the
+roofline), the end-to-end call with pinned host buffers (copies inside the
+timed region), decode steps replayed from a CUDA graph (1, 8, 32, 64
+tokens), a token sweep (128 ... 65536), and the CPU oracle on a bounded
+sample of the same workload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -42,7 +44,7 @@ METRIC = "indexer-Q tokens/s at M=4632; FP8 quantizer GB/s vs HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0            # nominal dense ratio (4.5 / 2.25 PFLOP/s)
-ORACLE_SAMPLE_ROWS = 1024      # rows of the prefill workload per oracle timing
+ORACLE_SAMPLE_ROWS = 4632      # rows of the prefill workload per oracle timing (all of it)
 
 
 def parse():
@@ -237,31 +239,28 @@ def run_ours(args):
     xs = torch.empty((3, (M + 3) // 4 * 4), dtype=torch.int32, device=dev)
     q = torch.empty((M, N_Q // 2), dtype=torch.uint8, device=dev)
     s = torch.empty((M, N_Q // 32), dtype=torch.uint8, device=dev)
+    work = torch.empty(iq.prepare_q_workspace_bytes(M), dtype=torch.uint8, device=dev)
 
     def step():
-        iq.fp8_quant_1x128_ue8m0(lat, y=xq, scales=xs)
-        iq.gemm_rope_hadamard_fp4(xq, xs, w, ws, p, q_fp4=q, q_sf=s)
+        # iq_prepare_q: the quantizer, then the fused GEMM as its programmatic
+        # dependent (no host or event work between the two launches).
+        iq.prepare_q(lat, w, ws, p, q_fp4=q, q_sf=s, workspace=work)
 
     for _ in range(max(3, args.warmup)):
         step()
     barrier()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     clocks = ClockSampler(local).__enter__()
-    if True:
-        barrier()
-        t_wall = time.perf_counter()
-        for i in range(args.steps):
-            flush_l2()
-            ev[i][0].record(stream)
-            iq.fp8_quant_1x128_ue8m0(lat, y=xq, scales=xs)
-            ev[i][1].record(stream)
-            iq.gemm_rope_hadamard_fp4(xq, xs, w, ws, p, q_fp4=q, q_sf=s)
-            ev[i][2].record(stream)
-        barrier()
-        t_wall = time.perf_counter() - t_wall
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    k1_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    k2_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    barrier()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush_l2()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     my_ms = sum(step_ms) / len(step_ms)
     t = torch.tensor([my_ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -269,7 +268,27 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     ms_per_step = float(t.item())
     value = world * M / (ms_per_step * 1e-3)
-    k2_avg_ms = sum(k2_ms) / len(k2_ms)
+
+    # The fused GEMM's own launch duration (for the roofline): the same
+    # launches with events around the GEMM alone (the quantizer runs first,
+    # outside the interval; W is not in L2, the FP8 latent is, as in a step).
+    k2ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in k2ev:
+        flush_l2()
+        iq.fp8_quant_1x128_ue8m0(lat, y=xq, scales=xs)
+        a.record(stream)
+        iq.gemm_rope_hadamard_fp4(xq, xs, w, ws, p, q_fp4=q, q_sf=s)
+        b.record(stream)
+    torch.cuda.synchronize()
+    k2_avg_ms = sum(a.elapsed_time(b) for a, b in k2ev) / len(k2ev)
+    k1ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in k1ev:
+        flush_l2()
+        a.record(stream)
+        iq.fp8_quant_1x128_ue8m0(lat, y=xq, scales=xs)
+        b.record(stream)
+    torch.cuda.synchronize()
+    k1_avg_ms = sum(a.elapsed_time(b) for a, b in k1ev) / len(k1ev)
 
     hbm_peak, bf16_peak, peak_kind = load_peaks()
     fp8_peak_tflops = bf16_peak * FP8_OVER_BF16
@@ -303,6 +322,123 @@ def run_ours(args):
                  "roofline": {"kernel": "quant_1x128_kernel", "bound": "hbm", "achieved": q_gbs, "peak": hbm_peak,
                               "unit": "GB/s", "frac": q_gbs / hbm_peak, "traffic": kernel_traffic("quant_1x128_kernel"),
                               "peak_source": peak_kind, "bytes_per_launch": q_bytes}}
+
+    # ------------------------------------------- decode under graph replay
+    # Decode steps (N(0,1) latent, random positions) replayed from a CUDA
+    # graph, per token count and per route (the small-M swapped-operand
+    # kernel, the default for M <= 64, and the CTA-pair kernel): once with W
+    # hot in L2 (the same W every call, 1000 calls), once with W rotated over
+    # 24 copies (302 MB, more than twice L2), so that every call reads W from
+    # HBM.
+    n_rot = 24
+    w_rot = [w.clone() for _ in range(n_rot)]
+
+    def graph_us_per_call(calls, total):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        for c in calls:
+            c()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for c in calls:
+                    c()
+        reps = max(1, total // len(calls))
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        del g
+        return a.elapsed_time(b) * 1e3 / (reps * len(calls))
+
+    decode = {"default_route_max_tokens": iq.small_m_threshold()}
+    for Md in (1, 8, 32, 64):
+        xd, _, _, pd = W.decode_chain(Md)
+        lat_d = torch.from_numpy(xd.view(np.int16)).view(torch.bfloat16).to(dev)
+        pos_d = torch.from_numpy(pd).to(dev)
+        q_d = torch.empty((Md, N_Q // 2), dtype=torch.uint8, device=dev)
+        s_d = torch.empty((Md, N_Q // 32), dtype=torch.uint8, device=dev)
+        work_d = torch.empty(iq.prepare_q_workspace_bytes(Md), dtype=torch.uint8, device=dev)
+
+        def call(wt):
+            return lambda: iq.prepare_q(lat_d, wt, ws, pos_d, q_fp4=q_d, q_sf=s_d, workspace=work_d)
+
+        entry = {}
+        for route, threshold in (("small_m", iq.SMALL_M_MAX), ("cta_pair", 0)):
+            old = iq.set_small_m_threshold(threshold)
+            try:
+                hot = graph_us_per_call([call(w)], 1000)
+                cold = graph_us_per_call([call(wt) for wt in w_rot], 1000)
+            finally:
+                iq.set_small_m_threshold(old)
+            entry[route] = {"us_per_step_w_in_l2": hot, "us_per_step_w_from_hbm": cold,
+                            "w_read_gbs_from_hbm": 12.58e6 / (cold * 1e-6) / 1e9,
+                            "w_read_frac_of_hbm": 12.58e6 / (cold * 1e-6) / 1e9 / hbm_peak}
+        default = "small_m" if Md <= decode["default_route_max_tokens"] else "cta_pair"
+        entry["tokens_per_s"] = Md / (entry[default]["us_per_step_w_in_l2"] * 1e-6)
+        decode[str(Md)] = entry
+    del w_rot
+
+    # ------------------------------------------------------ token sweep
+    # Chain and quantizer-alone at each sweep point (L2 flushed before each
+    # timed launch); inputs generated on the device: N(0,1), 0.5% x100
+    # outliers, random positions.
+    sweep = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4)
+    for Ms in (128, 512, 1024, 4632, 16384, 65536):
+        def bf16_input(rows, cols):
+            t = torch.randn((rows, cols), generator=gen, device=dev)
+            hit = torch.rand((rows, cols), generator=gen, device=dev) < 0.005
+            return torch.where(hit, t * 100.0, t).to(torch.bfloat16)
+        lat_s = bf16_input(Ms, K_LATENT)
+        pos_s = torch.randint(0, 163840, (Ms,), generator=gen, device=dev, dtype=torch.int32)
+        q_s = torch.empty((Ms, N_Q // 2), dtype=torch.uint8, device=dev)
+        s_s = torch.empty((Ms, N_Q // 32), dtype=torch.uint8, device=dev)
+        work_s = torch.empty(iq.prepare_q_workspace_bytes(Ms), dtype=torch.uint8, device=dev)
+        reps = 10 if Ms >= 16384 else 20
+        for _ in range(3):
+            iq.prepare_q(lat_s, w, ws, pos_s, q_fp4=q_s, q_sf=s_s, workspace=work_s)
+        chain_t = []
+        for _ in range(reps):
+            flush_l2()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            iq.prepare_q(lat_s, w, ws, pos_s, q_fp4=q_s, q_sf=s_s, workspace=work_s)
+            b.record()
+            chain_t.append((a, b))
+        torch.cuda.synchronize()
+        c_ms = sum(a.elapsed_time(b) for a, b in chain_t) / reps
+        del lat_s, q_s, s_s, work_s
+        xq_in = bf16_input(Ms, K_QUANT)
+        yq = torch.empty((Ms, K_QUANT), dtype=torch.uint8, device=dev)
+        sq = torch.empty(((K_QUANT + 511) // 512, (Ms + 3) // 4 * 4), dtype=torch.int32, device=dev)
+        for _ in range(3):
+            iq.fp8_quant_1x128_ue8m0(xq_in, y=yq, scales=sq)
+        qt = []
+        for _ in range(reps):
+            flush_l2()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            iq.fp8_quant_1x128_ue8m0(xq_in, y=yq, scales=sq)
+            b.record()
+            qt.append((a, b))
+        torch.cuda.synchronize()
+        qs_ms = sum(a.elapsed_time(b) for a, b in qt) / reps
+        qbytes = Ms * K_QUANT * 3 + sq.numel() * 4
+        del xq_in, yq, sq
+        flops = Ms * FLOPS_PER_TOKEN
+        sweep[str(Ms)] = {
+            "chain_us": c_ms * 1e3, "tokens_per_s": Ms / (c_ms * 1e-3),
+            "chain_tflops": flops / (c_ms * 1e-3) / 1e12, "chain_frac_of_fp8_peak": flops / (c_ms * 1e-3) / 1e12 / fp8_peak_tflops,
+            "quant7168_us": qs_ms * 1e3, "quant7168_gbs": qbytes / (qs_ms * 1e-3) / 1e9,
+            "quant7168_frac_of_hbm": qbytes / (qs_ms * 1e-3) / 1e9 / hbm_peak}
 
     # ------------------------------------------ end to end through the C ABI
     h_lat = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -340,7 +476,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         secs = oracle_sample_seconds(ORACLE_SAMPLE_ROWS)
         cpu = {"value": ORACLE_SAMPLE_ROWS / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"first {ORACLE_SAMPLE_ROWS} tokens of the 4632-token prefill workload, FP64 numpy, "
+               "sample": f"all {ORACLE_SAMPLE_ROWS} tokens of the prefill workload, FP64 numpy, "
                          f"one thread ({secs:.1f} s)"}
 
     if rank == 0:
@@ -357,7 +493,8 @@ def run_ours(args):
             "roofline": roofline, "quantizer": quantizer, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": 2 * args.steps,
             "clocks": clocks.summary(),
-            "k1_chain_avg_ms": sum(k1_ms) / len(k1_ms), "wall_s_timed": t_wall,
+            "k1_chain_avg_ms": k1_avg_ms, "wall_s_timed": t_wall,
+            "decode": decode, "sweep": sweep,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

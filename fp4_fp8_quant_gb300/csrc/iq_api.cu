@@ -29,6 +29,7 @@ struct DeviceInfo {
 std::mutex g_setup_mutex;
 DeviceInfo g_devices[kMaxDevices];
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int> g_small_m_max{iq::kSmallMMax};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -48,7 +49,8 @@ iq_status device_setup(int* max_pairs) {
     }
     if (major != 10 || minor != 3) {
       d.status = IQ_ERR_ARCH;
-    } else if (iq::gemm_setup_device(&d.max_pairs) != cudaSuccess || d.max_pairs < 1) {
+    } else if (iq::gemm_setup_device(&d.max_pairs) != cudaSuccess || d.max_pairs < 1 ||
+               iq::small_m_setup_device() != cudaSuccess) {
       d.status = IQ_ERR_CUDA;
     } else {
       d.status = IQ_OK;
@@ -100,14 +102,6 @@ iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq,
                      const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf, float* q_pre, int max_pairs,
                      cudaStream_t stream) {
   static const iq::RopeTurns rope = make_rope_turns();
-  // X: this CTA's 128 token rows per K-block; W: one head (128 rows) per
-  // CTA of the pair; Q codes: one head of 128 rows x 64 bytes per store.
-  CUtensorMap tm_x, tm_w, tm_q;
-  if (!encode_2d_u8(&tm_x, xq, iq::kLatentDim, static_cast<uint64_t>(M), 128, 128) ||
-      !encode_2d_u8(&tm_w, wq, iq::kLatentDim, iq::kQDim, 128, 256 / iq::gemm_pair_size()) ||
-      !encode_2d_u8(&tm_q, q_fp4, iq::kQDim / 2, static_cast<uint64_t>(M), 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) {
-    return IQ_ERR_CUDA;
-  }
   iq::GemmArgs a;
   a.x_sf = x_sf;
   a.w_sf = wq_sf;
@@ -122,6 +116,23 @@ iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq,
   a.num_pair_tiles = a.num_m_pairs * (iq::kQDim / 256);
   a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   a.rope = rope;
+  CUtensorMap tm_x, tm_w, tm_q;
+  if (M <= g_small_m_max.load(std::memory_order_relaxed)) {
+    // Small-M route: the M token rows per K-block (a box of exactly M rows);
+    // one head (128 rows) of W per CTA.
+    if (!encode_2d_u8(&tm_x, xq, iq::kLatentDim, static_cast<uint64_t>(M), 128, static_cast<uint32_t>(M)) ||
+        !encode_2d_u8(&tm_w, wq, iq::kLatentDim, iq::kQDim, 128, iq::kHeadDim)) {
+      return IQ_ERR_CUDA;
+    }
+    return iq::launch_small_m_rope_hadamard_fp4(tm_x, tm_w, a, stream) == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
+  }
+  // X: this CTA's 128 token rows per K-block; W: one head (128 rows) per
+  // CTA of the pair; Q codes: one head of 128 rows x 64 bytes per store.
+  if (!encode_2d_u8(&tm_x, xq, iq::kLatentDim, static_cast<uint64_t>(M), 128, 128) ||
+      !encode_2d_u8(&tm_w, wq, iq::kLatentDim, iq::kQDim, 128, 256 / iq::gemm_pair_size()) ||
+      !encode_2d_u8(&tm_q, q_fp4, iq::kQDim / 2, static_cast<uint64_t>(M), 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) {
+    return IQ_ERR_CUDA;
+  }
   return iq::launch_gemm_rope_hadamard_fp4(tm_x, tm_w, tm_q, a, max_pairs, stream) == cudaSuccess ? IQ_OK
                                                                                                    : IQ_ERR_CUDA;
 }
@@ -177,13 +188,22 @@ const char* iq_status_str(iq_status s) {
 }
 
 iq_status iq_device_status(uint32_t* flags, int reset) {
-  uint32_t v = 0;
-  if (iq::read_device_status(&v, reset != 0) != cudaSuccess) return IQ_ERR_CUDA;
+  uint32_t v = 0, w = 0;
+  if (iq::read_device_status(&v, reset != 0) != cudaSuccess || iq::read_small_m_status(&w, reset != 0) != cudaSuccess)
+    return IQ_ERR_CUDA;
+  v |= w;
   if (flags) *flags = v;
   return v ? IQ_ERR_TIMEOUT : IQ_OK;
 }
 
 void iq_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs); }
+
+int iq_set_small_m_threshold(int max_tokens) {
+  const int v = max_tokens < 0 ? 0 : (max_tokens > iq::kSmallMMax ? iq::kSmallMMax : max_tokens);
+  return g_small_m_max.exchange(v);
+}
+
+int iq_small_m_threshold(void) { return g_small_m_max.load(); }
 
 size_t iq_fp8_scale_words(int M, int K) {
   if (M <= 0 || K <= 0) return 0;

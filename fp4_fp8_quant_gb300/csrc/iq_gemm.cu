@@ -56,6 +56,7 @@
 
 #include <cstdint>
 
+#include "iq_fp4.cuh"
 #include "iq_internal.h"
 #include "iq_ptx.cuh"
 
@@ -95,21 +96,9 @@ constexpr int kNumBars = 2 * kStages + 4 + 3;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 
-constexpr float kInvSqrt128 = 0.0883883476483184405501f;
-constexpr float kTwoPi = 6.28318530717958647692f;
-
 __device__ __forceinline__ void fail(volatile uint32_t* abort_flag, uint32_t bit) {
   atomicOr(&g_iq_status, bit);
   *abort_flag = 1u;
-}
-
-// Scale exponent of the FP4 stage: smallest e with 6 * 2^e >= max(a, 1e-4).
-// With a = (1 + f) 2^E and 6 = 1.5 * 2^2: e = E - 2 when f <= 0.5, else E - 1.
-__device__ __forceinline__ int fp4_scale_exponent(float a) {
-  a = fmaxf(a, kAmaxFloor);
-  const uint32_t bits = __float_as_uint(a);
-  const int E = static_cast<int>(bits >> 23) - 127;
-  return E - 2 + ((bits & 0x7FFFFFu) > 0x400000u ? 1 : 0);
 }
 
 // RoPE, Hadamard, FP4 for one (token, head).  p[j] holds dims (2j, 2j+1) of
@@ -183,7 +172,7 @@ __device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int hea
       amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
     }
     const int e = fp4_scale_exponent(amax * kInvSqrt128);
-    const float k = __uint_as_float(static_cast<uint32_t>(127 - e) << 23) * kInvSqrt128;
+    const float k = fp4_code_factor(e);
     const uint64_t kk = f2_pack(k, k);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {

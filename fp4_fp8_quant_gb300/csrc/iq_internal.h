@@ -19,6 +19,7 @@ constexpr int kHeadDim = 128;
 constexpr int kQDim = kNumHeads * kHeadDim;   // 8192
 constexpr int kNumKBlocks = kLatentDim / 128; // 12
 constexpr int kScaleGroups = kNumKBlocks / 4; // 3 packed int32 words per row
+constexpr int kSmallMMax = 64;                // most tokens the small-M kernel takes
 
 // RoPE frequencies of the 32 NeoX pairs, in turns per position unit:
 // 10000^(-i/32) / (2 pi), split into a float32 head and tail.
@@ -63,7 +64,14 @@ int gemm_pair_size();
 cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
                                           const GemmArgs& args, int max_pairs, cudaStream_t stream);
 
-// Device status word access (synchronous).
+// The small-M (swapped-operand) kernel: M <= kSmallMMax tokens, one launch
+// of 64 clusters of two CTAs (one per K half).
+cudaError_t small_m_setup_device();
+cudaError_t launch_small_m_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const GemmArgs& args,
+                                             cudaStream_t stream);
+
+// Device status words of the large-M and small-M kernels (synchronous).
 cudaError_t read_device_status(uint32_t* flags, bool reset);
+cudaError_t read_small_m_status(uint32_t* flags, bool reset);
 
 }  // namespace iq

@@ -167,6 +167,30 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split form of the cluster barrier: every thread of every CTA of the cluster
+// arrives once and then waits once.  A relaxed arrive orders nothing: it only
+// says that this CTA is running (so its shared memory may be addressed); a
+// release arrive makes this thread's earlier writes, shared::cluster stores
+// included, visible to every thread that then completes the (acquire) wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Asynchronous 32-bit store into the shared memory of a CTA of the cluster
+// (addresses from mapa_shared): its 4 bytes are counted as completed
+// transactions on `bar`, an mbarrier in the same CTA as `addr`.  A thread that
+// observes that barrier's phase complete sees the data; the storing thread
+// needs no release fence.
+__device__ __forceinline__ void st_async_cluster_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+               "r"(__float_as_uint(v)), "r"(bar)
+               : "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -361,6 +385,19 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float* v) {
       "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
       : "=r"(r)
       : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// Four floats -> four E2M1 codes (RNE, saturating) in 16 bits: element i in
+// bits 4i..4i+3.
+__device__ __forceinline__ uint32_t cvt_e2m1x4(float v0, float v1, float v2, float v3) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 b0, b1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "mov.b16 %0, {b0, b1};\n\t}"
+      : "=h"(r)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
   return r;
 }
 

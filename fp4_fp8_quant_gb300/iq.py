@@ -18,6 +18,7 @@ LATENT_DIM = 1536
 N_HEADS = 64
 HEAD_DIM = 128
 Q_DIM = 8192
+SMALL_M_MAX = 64
 
 _STATUS = {0: "IQ_OK", -1: "IQ_ERR_ARG", -2: "IQ_ERR_ALIGN", -3: "IQ_ERR_SHAPE", -4: "IQ_ERR_ARCH",
            -5: "IQ_ERR_CUDA", -6: "IQ_ERR_WORKSPACE", -7: "IQ_ERR_TIMEOUT"}
@@ -37,6 +38,8 @@ SIGNATURES = {
     "iq_prepare_q_debug": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "iq_gemm_rope_hadamard_fp4": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _P, _P]),
     "iq_prepare_q_static": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
+    "iq_set_small_m_threshold": (_I, [_I]),
+    "iq_small_m_threshold": (_I, []),
 }
 
 _lib = None
@@ -198,3 +201,13 @@ def device_status(reset: bool = False) -> int:
 
 def set_wait_timeout_ns(ns: int) -> None:
     lib().iq_set_wait_timeout_ns(int(ns))
+
+
+def set_small_m_threshold(max_tokens: int) -> int:
+    """Largest M routed to the small-M (swapped-operand) kernel, clamped to
+    [0, 64]; returns the previous value."""
+    return int(lib().iq_set_small_m_threshold(int(max_tokens)))
+
+
+def small_m_threshold() -> int:
+    return int(lib().iq_small_m_threshold())

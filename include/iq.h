@@ -76,6 +76,22 @@ iq_status iq_device_status(uint32_t* flags, int reset);
  * thread. */
 void iq_set_wait_timeout_ns(uint64_t ns);
 
+/* Token-count route of the fused GEMM (operation 2).  Calls with
+ * 1 <= M <= threshold run the small-M kernel, which swaps the MMA operands
+ * (the weights on the MMA's M side, the tokens on its N side), the variant the
+ * TensorRT-LLM PR routes small token counts to (dispatch thresholds); larger
+ * M runs the persistent CTA-pair kernel.  Both compute the same operation;
+ * their float32 sums may round differently, within the error the parity rules
+ * of operation 2 allow.  The threshold is clamped to [0, IQ_SMALL_M_MAX]; 0
+ * sends every M to the CTA-pair kernel.  The default is IQ_SMALL_M_MAX.
+ * Process-wide; applies to later calls from any thread (a CUDA graph keeps
+ * the route it was captured with).  Returns the previous threshold. */
+#define IQ_SMALL_M_MAX 64
+int iq_set_small_m_threshold(int max_tokens);
+
+/* The current threshold (see iq_set_small_m_threshold). */
+int iq_small_m_threshold(void);
+
 /* ------------------------------------------------------------------------
  * 1. FP8 1x128 quantizer with packed UE8M0 scales.
  * ------------------------------------------------------------------------ */
@@ -144,8 +160,11 @@ size_t iq_prepare_q_workspace(int M);
  *   workspace    caller scratch of at least iq_prepare_q_workspace(M) bytes,
  *                256-byte aligned; its contents on return are the FP8 latent
  *                and its packed scales (operation 1's outputs).
- * M == 0 returns IQ_OK without a launch.  Two kernel launches (the quantizer
- * and the fused GEMM), back to back on `stream`. */
+ * M == 0 returns IQ_OK without a launch.  Two kernel launches, back to back
+ * on `stream`: the quantizer, then the fused GEMM kernel of M's route (see
+ * iq_set_small_m_threshold), launched as the quantizer's programmatic
+ * dependent so that its set-up (and, on the small-M route, its weight loads)
+ * overlap the quantizer. */
 iq_status iq_prepare_q(const void* latent_bf16, int M,
                        const void* wq_e4m3, const uint8_t* wq_sf,
                        const int32_t* positions,

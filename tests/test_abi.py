@@ -80,3 +80,19 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(iq, "_lib", None)
     with pytest.raises(ImportError):
         iq.lib()
+
+
+def test_small_m_threshold_is_clamped_and_restored(lib):
+    """The token-count route switch is host state only: no device needed."""
+    old = lib.iq_small_m_threshold()
+    assert old == 64
+    try:
+        assert lib.iq_set_small_m_threshold(8) == 64
+        assert lib.iq_small_m_threshold() == 8
+        lib.iq_set_small_m_threshold(1000)
+        assert lib.iq_small_m_threshold() == 64
+        lib.iq_set_small_m_threshold(-5)
+        assert lib.iq_small_m_threshold() == 0
+    finally:
+        lib.iq_set_small_m_threshold(old)
+    assert lib.iq_small_m_threshold() == old
