@@ -23,6 +23,7 @@
 
 #include <cstdint>
 
+#include "iq_fp8.cuh"
 #include "iq_internal.h"
 #include "iq_ptx.cuh"
 
@@ -38,31 +39,6 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;
-}
-
-// |x| of two packed BF16 values, as unsigned 16-bit lanes, max-reduced.
-__device__ __forceinline__ uint32_t abs_max_bf16x2(uint32_t acc, uint32_t v) {
-  return __vmaxu2(acc, v & 0x7FFF7FFFu);
-}
-
-// Scale exponent e of the FP8 stage: the smallest integer with
-// 448 * 2^e >= max(amax, 1e-4).  With a = (1 + f) 2^E, 448 = 1.75 * 2^8:
-// e = E - 8 when f <= 0.75 (mantissa bits <= 0x600000), else E - 7.
-__device__ __forceinline__ int fp8_scale_exponent(float amax) {
-  const float a = fmaxf(amax, kAmaxFloor);
-  const uint32_t bits = __float_as_uint(a);
-  const int E = static_cast<int>(bits >> 23) - 127;
-  return E - 8 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
-}
-
-__device__ __forceinline__ uint32_t quant_pair(uint32_t bf2, float inv) {
-  const float lo = __uint_as_float(bf2 << 16) * inv;
-  const float hi = __uint_as_float(bf2 & 0xFFFF0000u) * inv;
-  return cvt_e4m3x2(lo, hi);
-}
-
-__device__ __forceinline__ uint32_t quant_quad(uint32_t a, uint32_t b, float inv) {
-  return quant_pair(a, inv) | (quant_pair(b, inv) << 16);
 }
 
 __global__ void __launch_bounds__(kThreads) quant_1x128_kernel(const uint16_t* __restrict__ x, int M, int K,
@@ -101,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) quant_1x128_kernel(const uint16_t* _
   const float amax = __uint_as_float(m1 << 16);
 
   const int e = fp8_scale_exponent(amax);
-  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);   // 2^-e, exact
+  const float inv = fp8_inv_scale(e);
   if (active) {
     uint4 out;
     out.x = quant_quad(a.x, a.y, inv);
