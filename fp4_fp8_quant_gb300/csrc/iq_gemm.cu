@@ -298,8 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int m = m0 + c * 32 + lane;
-          ra[g][c] =
-              m < args.m_al ? static_cast<uint32_t>(__ldg(args.x_sf + static_cast<long long>(g) * args.m_al + m)) : 0u;
+          ra[g][c] = m < args.m_al ? ld_dependent_u32(args.x_sf + static_cast<long long>(g) * args.m_al + m) : 0u;
         }
         if (new_heads(pt)) {
 #pragma unroll
@@ -457,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int pt = first_pt; pt < end_pt; ++pt, ++local) {
       const int row = tile_m0(pt) + trow;
       const int head = tile_n(pt) * 2 + half;
-      const int pos = row < args.M ? __ldg(args.pos + row) : 0;   // in flight during the wait
+      const int pos = row < args.M ? static_cast<int>(ld_dependent_u32(args.pos + row)) : 0;   // in flight during the wait
       // The previous tile's bulk stores must have read the staging tile
       // before anyone overwrites it.
       if (store_issuer) tma_store_wait_read();

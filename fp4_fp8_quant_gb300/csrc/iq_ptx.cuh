@@ -120,6 +120,17 @@ __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bu
 // completed and their memory is visible; returns at once otherwise.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// 32-bit load of data the preceding grid wrote, for use after
+// grid_dependency_wait(): a volatile relaxed load at GPU scope, which the
+// compiler keeps below the wait and which does not use the read-only data
+// path (__ldg / ld.global.nc may be hoisted above the wait and may serve a
+// line that the preceding grid is still writing).
+__device__ __forceinline__ uint32_t ld_dependent_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(reinterpret_cast<uint64_t>(p)) : "memory");
+  return v;
+}
+
 // Lets the dependent grid of the stream be scheduled before this one ends.
 __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int m = c * 32 + lane;
-        r[c] = m < M ? static_cast<uint32_t>(__ldg(args.x_sf + static_cast<long long>(g) * args.m_al + m)) : 0u;
+        r[c] = m < M ? ld_dependent_u32(args.x_sf + static_cast<long long>(g) * args.m_al + m) : 0u;
       }
       *reinterpret_cast<uint4*>(sSfb + g * 128 + lane * 4) = make_uint4(r[0], r[1], r[2], r[3]);
     }
@@ -270,6 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // tokens t = 2 (warp + 8 j) + K half, their positions (lanes 0..15 rotate),
   // and the RoPE frequencies of dims 4 (l % 8) + k in turns per position unit
   // (lanes 0..7 hold the first element of each NeoX pair, 8..15 the second).
+  // Positions are read after the wait like every other input (besides W and
+  // its scales); the epilogue warps are idle until the MMAs complete anyway.
+  grid_dependency_wait();
   int tok_index[kTokPerWarp];
   bool tok_valid[kTokPerWarp];
   float tok_pos[kTokPerWarp];
@@ -277,7 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int j = 0; j < kTokPerWarp; ++j) {
     tok_index[j] = 2 * (warp + j * kWarps) + static_cast<int>(rank);
     tok_valid[j] = tok_index[j] < M;
-    tok_pos[j] = (tok_valid[j] && lane < 16) ? static_cast<float>(__ldg(args.pos + tok_index[j])) : 0.f;
+    tok_pos[j] =
+        (tok_valid[j] && lane < 16) ? static_cast<float>(static_cast<int>(ld_dependent_u32(args.pos + tok_index[j]))) : 0.f;
   }
   float fhi[4], flo[4];
 #pragma unroll

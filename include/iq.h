@@ -164,7 +164,15 @@ size_t iq_prepare_q_workspace(int M);
  * on `stream`: the quantizer, then the fused GEMM kernel of M's route (see
  * iq_set_small_m_threshold), launched as the quantizer's programmatic
  * dependent so that its set-up (and, on the small-M route, its weight loads)
- * overlap the quantizer. */
+ * overlap the quantizer.
+ *
+ * Ordering: the GEMM kernel of the small-M route reads wq_e4m3 and wq_sf
+ * before the kernel launched just before it on `stream` has completed (that
+ * kernel is the quantizer for iq_prepare_q; for iq_gemm_rope_hadamard_fp4 it
+ * is whatever the caller launched last, and the overlap happens only if that
+ * kernel allows programmatic dependents).  The weights must therefore not be
+ * written by the immediately preceding kernel.  Every other input is read
+ * after that kernel has completed. */
 iq_status iq_prepare_q(const void* latent_bf16, int M,
                        const void* wq_e4m3, const uint8_t* wq_sf,
                        const int32_t* positions,
