@@ -16,12 +16,11 @@
 //     B side, N = 64) over one half of K
 //     (6 of the 12 K-blocks) with the 1-SM MMA (tcgen05 kind::mxf8f6f4
 //     block_scale); the accumulators are FP32 in tensor memory;
-//   * several MMA issuers: on GB300 one thread issues at most about one
-//     tcgen05.mma per 160 cycles (measured; the same for N = 64 and 128, for
-//     the 1-SM and the 2-SM form, with or without block scaling), a fifth of
-//     the tensor rate at N = 64.  The K-blocks are dealt to three threads,
-//     each accumulating into its own 64 TMEM columns, and the epilogue adds
-//     the three partial sums;
+//   * several MMA issuers: with one issuing thread the 24 MMAs of a CTA (32
+//     cycles of tensor work each at N = 64) measured 100-160 cycles apart;
+//     with the K-blocks dealt to three threads, each accumulating into its
+//     own 64 TMEM columns, the whole MMA phase took a third of the time.  The
+//     epilogue adds the three partial sums;
 //   * the token tile of a K-block is loaded as exactly M rows: rows M..63 of
 //     the B side keep whatever shared memory held, which reaches only
 //     accumulator columns M..63 (column n depends on B row n alone), and
