@@ -62,6 +62,22 @@ def dist_info():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's `value` (the slowest rank's step time);
+    needs the default process group when world > 1."""
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Units all ranks processed per second, timed by the slowest rank."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -261,13 +277,8 @@ def run_ours(args):
     barrier()
     t_wall = time.perf_counter() - t_wall
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    my_ms = sum(step_ms) / len(step_ms)
-    t = torch.tensor([my_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_per_step = float(t.item())
-    value = world * M / (ms_per_step * 1e-3)
+    ms_per_step = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
+    value = whole_job_rate(M, world, ms_per_step)
 
     # The fused GEMM's own launch duration (for the roofline): the same
     # launches with events around the GEMM alone (the quantizer runs first,
