@@ -72,6 +72,7 @@ constexpr int BK = 128;
 constexpr int kPair = 2;
 constexpr uint16_t kPairMask = 0x3;
 constexpr int kStages = 6;
+static_assert(kNumKBlocks == 2 * kStages, "a tile is two passes over the ring (static phases in the MMA loop)");
 constexpr int kABytes = BM * BK;                 // 16 KB: this CTA's token rows
 constexpr int kBBytes = (BN / kPair) * BK;       // 16 KB: this CTA's head of W
 constexpr int kPairStageTx = kPair * (kABytes + kBBytes);   // bytes landing per stage, both CTAs
@@ -383,7 +384,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------- MMA issuer (leader)
     if (lane == 0) {
       if (leader) {
-        uint32_t stage = 0, phase = 0;
         int local = 0;
         bool ok = true;
         const uint64_t adesc0 = smem_desc_sw128(smem_u32(sA));
@@ -410,16 +410,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tc_commit_pair(&sf_empty[buf], kPairMask);
-          // The K loop does little between MMAs.  TMA data needs no tcgen05
+          // The K loop does little between MMAs: a tile is exactly two
+          // passes over the ring, so every stage index, barrier phase, scale
+          // ID and descriptor offset below is a compile-time constant and the
+          // issuing thread spends few instructions per stage (it shares its
+          // scheduler with two epilogue warps).  TMA data needs no tcgen05
           // fence: the barrier's transaction completion orders it.
+#pragma unroll
           for (int kb = 0; kb < kNumKBlocks; ++kb) {
-            if (!mbar_wait(&full[stage], phase, timeout)) {
+            const int s = kb % kStages;
+            if (!mbar_wait(&full[s], static_cast<uint32_t>(kb / kStages) & 1u, timeout)) {
               fail(abort_flag, kStatusMmaWait);
               ok = false;
               break;
             }
-            const uint64_t adesc = adesc0 + static_cast<uint64_t>(stage * (kABytes >> 4));
-            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * (kBBytes >> 4));
+            const uint64_t adesc = adesc0 + static_cast<uint64_t>(s * (kABytes >> 4));
+            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(s * (kBBytes >> 4));
             const uint32_t sfid = static_cast<uint32_t>(kb & 3);
             const uint32_t idesc = idesc0 | (sfid << 4) | (sfid << 29);
             const uint32_t sf_off = 8u * static_cast<uint32_t>(kb >> 2);
@@ -429,11 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_mma_mxf8_pair(tmem + kAccCol, adesc + 2 * k, bdesc + 2 * k, idesc, tmem + kSfaCol + sf_off,
                                tmem + kSfbCol + sf_off, (kb | k) != 0);
             }
-            tc_commit_pair(&empty[stage], kPairMask);   // frees the stage in both CTAs
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1;
-            }
+            tc_commit_pair(&empty[s], kPairMask);   // frees the stage in both CTAs
           }
           if (ok) tc_commit_pair(tmem_full, kPairMask);
         }
