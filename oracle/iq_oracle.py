@@ -37,6 +37,16 @@ Readings where the pages are silent (named A1..A10 in the design notes):
   The FP4 rounding decision is taken on the pre-quant value rounded to float32,
   the precision the CUDA path decides in.
 
+FP4 output variants (the pages fix only MXFP4 with UE8M0 scales; these are the
+alternatives the design notes list, each selectable on the CUDA path):
+  "mx"      the rule above (A9: ceil, never saturates);
+  "mx_ocp"  [OCP] MX v1.0 shared-scale rule: X = 2^(floor(log2 amax) - emax)
+            with emax = 2 for E2M1, elements saturating at 6 (A13);
+  "nv"      NVFP4-style: 1x16 blocks, the scale an E4M3 value (A14): per-tensor
+            scale 1; s = E4M3 round-to-nearest of float32(amax / 6), raised
+            to 2^-9 (the smallest positive E4M3) when it rounds to zero; codes
+            E2M1(float32(z * float32(1 / s))); scales [M][64][8] E4M3 bytes.
+
 Parity of A1, A8 and A9 (the absolute scale choices) is pinned only by these
 readings: the pages do not state them.
 """
@@ -50,6 +60,9 @@ E2M1_MAX = 6.0
 AMAX_FLOOR = 1e-4          # A1 / A8
 FP8_BLOCK = 128            # 1x128 activation blocks [TS] Summary; [TRT] Walkthrough
 FP4_BLOCK = 32             # MXF8 sf_vec_size = 32 [TRT] review comment
+NVFP4_BLOCK = 16           # A14
+E4M3_MIN_POS = 2.0 ** -9   # smallest positive E4M3 value [OCP]
+FP4_FORMATS = ("mx", "mx_ocp", "nv")
 HEAD_DIM = 128
 ROPE_DIM = 64
 ROPE_THETA = 10000.0
@@ -279,6 +292,48 @@ def quantize_fp4_1x32(z: np.ndarray):
     return codes.reshape(M, D), (e + UE8M0_BIAS).astype(np.uint8)
 
 
+def ue8m0_exponent_ocp(amax: np.ndarray, floor: float = AMAX_FLOOR) -> np.ndarray:
+    """[OCP] MX v1.0 shared scale of an E2M1 block (A13): X = 2^e with
+    e = floor(log2(max(amax, floor))) - 2, emax(E2M1) = 2, so the block's
+    largest magnitude lands in [4, 8) before the elements saturate at 6."""
+    a = np.maximum(np.asarray(amax, dtype=np.float64), floor)
+    _, ex = np.frexp(a)                          # a = f * 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1
+    return ex.astype(np.int64) - 1 - 2
+
+
+def quantize_fp4_1x32_ocp(z: np.ndarray):
+    """quantize_fp4_1x32 with the [OCP] floor rule (A13).  Returns (codes
+    uint8 [M, D], scale bytes uint8 [M, D/32])."""
+    M, D = z.shape
+    b = z.reshape(M, D // FP4_BLOCK, FP4_BLOCK)
+    amax = np.abs(b).max(axis=2) if M else np.zeros((0, D // FP4_BLOCK))
+    e = ue8m0_exponent_ocp(amax)
+    codes = round_to_e2m1_codes(b * np.ldexp(1.0, -e)[..., None])
+    return codes.reshape(M, D), (e + UE8M0_BIAS).astype(np.uint8)
+
+
+def nvfp4_block_scale(amax_f32: np.ndarray) -> np.ndarray:
+    """E4M3 scale code of an NVFP4 block (A14): round-to-nearest-even of
+    float32(max(amax, floor) / 6) onto E4M3, or 2^-9 when that is zero."""
+    a = np.maximum(np.asarray(amax_f32, dtype=np.float32), np.float32(AMAX_FLOOR))
+    s = (a / np.float32(E2M1_MAX)).astype(np.float64)          # float32 division, then exact in float64
+    code = round_to_e4m3_codes(s)
+    return np.where(code == 0, np.uint8(1), code).astype(np.uint8)   # code 1 = 2^-9
+
+
+def quantize_nvfp4_1x16(z_f32: np.ndarray):
+    """NVFP4-style 1x16 blocks with E4M3 scales (A14) on float32 values.
+    Returns (codes uint8 [M, D], scale codes uint8 [M, D/16])."""
+    M, D = z_f32.shape
+    b = np.asarray(z_f32, dtype=np.float32).reshape(M, D // NVFP4_BLOCK, NVFP4_BLOCK)
+    amax = np.abs(b).max(axis=2) if M else np.zeros((0, D // NVFP4_BLOCK), np.float32)
+    sc = nvfp4_block_scale(amax)
+    r = (1.0 / decode_e4m3(sc)).astype(np.float32)           # float32(1 / s), correctly rounded
+    u = (b * r[..., None]).astype(np.float32)                 # float32 product
+    codes = round_to_e2m1_codes(u.astype(np.float64))
+    return codes.reshape(M, D), sc
+
+
 def pack_fp4(codes: np.ndarray) -> np.ndarray:
     """Two E2M1 codes per byte, element 2i in the low nibble (A10)."""
     return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
@@ -286,25 +341,34 @@ def pack_fp4(codes: np.ndarray) -> np.ndarray:
 
 # ----------------------------------------------------------------- the chain
 
-def prepare_q(latent_bits: np.ndarray, wq: np.ndarray, w_sb: np.ndarray, pos: np.ndarray):
+def prepare_q(latent_bits: np.ndarray, wq: np.ndarray, w_sb: np.ndarray, pos: np.ndarray, fmt: str = "mx"):
     """The second call of the library, end to end ([TRT] sequence diagram:
     quantize the latent to FP8 with UE8M0 scales, block-scaled GEMM with the
-    RoPE and FP4 epilogue, return packed FP4 Q and scales).
+    RoPE and FP4 epilogue, return packed FP4 Q and scales).  fmt picks the FP4
+    output variant (module docstring).
 
-    Returns (q_fp4 uint8 [M, 4096], q_sf uint8 [M, 256], z float64 [M, 8192])
-    where z is the pre-quant Q (after RoPE and Hadamard)."""
+    Returns (q_fp4 uint8 [M, 4096], q_sf uint8 [M, 256] ([M, 512] for "nv"),
+    z float64 [M, 8192]) where z is the pre-quant Q (after RoPE and
+    Hadamard)."""
     x = bf16_bits_to_f64(latent_bits)
     xq, x_sb = quantize_fp8_1x128(x)
     y = block_scaled_gemm(xq, x_sb, wq, w_sb)
     z = hadamard_heads(rope_neox(y, pos))
     z_decide = z.astype(np.float32).astype(np.float64)   # decision precision: float32
-    codes, q_sf = quantize_fp4_1x32(z_decide)
+    if fmt == "mx":
+        codes, q_sf = quantize_fp4_1x32(z_decide)
+    elif fmt == "mx_ocp":
+        codes, q_sf = quantize_fp4_1x32_ocp(z_decide)
+    elif fmt == "nv":
+        codes, q_sf = quantize_nvfp4_1x16(z_decide.astype(np.float32))
+    else:
+        raise ValueError(f"unknown FP4 format {fmt!r}")
     return pack_fp4(codes), q_sf, z
 
 
 def prequant_q_rows(latent_bits: np.ndarray, wq: np.ndarray, w_sb: np.ndarray,
-                    pos: np.ndarray, rows: np.ndarray):
+                    pos: np.ndarray, rows: np.ndarray, fmt: str = "mx"):
     """prepare_q on a subset of rows (rows are independent), for sampled checks
     of large problems."""
     rows = np.asarray(rows)
-    return prepare_q(latent_bits[rows], wq, w_sb, pos[rows])
+    return prepare_q(latent_bits[rows], wq, w_sb, pos[rows], fmt)

@@ -296,6 +296,91 @@ def test_fp4_invariants_and_packing():
     assert O.pack_fp4(codes).tolist() == [[0x21, 0x8F]]
 
 
+def _nearest_even_by_search(values: np.ndarray, grid: np.ndarray) -> np.ndarray:
+    """Index of the grid value nearest to each |value| (ties to the even index),
+    by exhaustive comparison; values above the grid saturate to its top."""
+    a = np.abs(np.asarray(values, np.float64))[..., None]
+    d = np.abs(grid[None, :] - a.reshape(-1, 1))
+    best = d.min(axis=1, keepdims=True)
+    ties = d == best
+    idx = np.where(ties.sum(axis=1) > 1, np.argmax(ties & (np.arange(len(grid)) % 2 == 0), axis=1),
+                   np.argmin(d, axis=1))
+    return idx.reshape(np.shape(values))
+
+
+def check_fp4_ocp_rule(seed=5):
+    """[OCP] MX v1.0: the shared exponent puts the block's largest magnitude in
+    [4, 8) (emax(E2M1) = 2, floor of log2), elements round to nearest-even on
+    the E2M1 grid and saturate at 6; floored blocks take floor(log2 1e-4) - 2 =
+    -16 (byte 111)."""
+    rng = np.random.default_rng(seed)
+    z = rng.standard_normal((8, 1024)) * np.exp(rng.uniform(-10, 10, (8, 1)))
+    z[1, :32] = 0.0
+    z[2, 32:64] = 31.999                               # amax just below the binade edge 2^5
+    z[2, 64:96] = np.ldexp(1.0, 5)                    # amax exactly a power of two
+    codes, sb = O.quantize_fp4_1x32_ocp(z)
+    e = sb.astype(np.int64) - 127
+    amax = np.abs(z.reshape(8, 32, 32)).max(axis=2)
+    floored = amax < O.AMAX_FLOOR
+    lo, hi = np.ldexp(4.0, e), np.ldexp(8.0, e)
+    assert np.all((amax[~floored] >= lo[~floored]) & (amax[~floored] < hi[~floored]))
+    assert np.all(sb[floored] == 111) and floored[1, 0]
+    assert e[2, 2] == 3 and e[2, 1] == 2
+    u = z.reshape(8, 32, 32) / np.ldexp(1.0, e)[..., None]
+    grid = O.e2m1_value_table()[:8]
+    want = _nearest_even_by_search(u, grid) | (np.signbit(u) << 3)
+    assert np.array_equal(codes.reshape(8, 32, 32), want.astype(np.uint8))
+    assert np.any((np.abs(u) > 6) & ((codes.reshape(8, 32, 32) & 7) == 7)), "saturation must occur"
+
+
+def check_nvfp4_rule(seed=6):
+    """A14: 1x16 blocks; the scale is the E4M3 value nearest float32(amax / 6)
+    (ties to even), 2^-9 when that is zero; codes are the E2M1 values nearest
+    float32(z * float32(1 / s)), saturating at 6."""
+    rng = np.random.default_rng(seed)
+    z = (rng.standard_normal((8, 512)) * np.exp(rng.uniform(-6, 6, (8, 1)))).astype(np.float32)
+    z[1, :16] = 0.0
+    z[2, 16:32] = np.float32(1e-5)
+    codes, sc = O.quantize_nvfp4_1x16(z)
+    e4 = O.e4m3_value_table()[:0x7F]
+    amax = np.maximum(np.abs(z.reshape(8, 32, 16)).max(axis=2), np.float32(O.AMAX_FLOOR))
+    target = (amax / np.float32(6.0)).astype(np.float64)
+    want_sc = _nearest_even_by_search(target, e4)
+    want_sc = np.where(want_sc == 0, 1, want_sc)
+    assert np.array_equal(sc, want_sc.astype(np.uint8))
+    assert sc[1, 0] == 1 and sc[2, 1] == 1
+    s = e4[sc]
+    r = np.float32(1.0) / s.astype(np.float32)
+    u = (z.reshape(8, 32, 16) * r[..., None]).astype(np.float32).astype(np.float64)
+    want = _nearest_even_by_search(u, O.e2m1_value_table()[:8]) | (np.signbit(u) << 3)
+    assert np.array_equal(codes.reshape(8, 32, 16), want.astype(np.uint8))
+
+
+def test_fp4_output_variants():
+    check_fp4_ocp_rule()
+    check_nvfp4_rule()
+    x, wq, wsf, pos = W.tiny_chain(3)
+    shapes = {f: tuple(a.shape for a in O.prepare_q(x, wq, wsf, pos, f)[:2]) for f in O.FP4_FORMATS}
+    assert shapes == {"mx": ((3, 4096), (3, 256)), "mx_ocp": ((3, 4096), (3, 256)), "nv": ((3, 4096), (3, 512))}
+
+
+def test_pins_catch_ocp_ceil_instead_of_floor(monkeypatch):
+    good = O.ue8m0_exponent_ocp
+
+    def bad(amax, floor=O.AMAX_FLOOR):   # the ceil rule in the floor rule's place
+        return O.ue8m0_exponent(amax, O.E2M1_MAX, floor)
+    _expect_fail(check_fp4_ocp_rule, monkeypatch, "ue8m0_exponent_ocp", bad)
+    assert good is O.ue8m0_exponent_ocp
+
+
+def test_pins_catch_nvfp4_scale_error(monkeypatch):
+    good = O.nvfp4_block_scale
+
+    def bad(amax_f32):   # amax / 4 instead of amax / 6
+        return good(np.asarray(amax_f32, np.float32) * np.float32(1.5))
+    _expect_fail(check_nvfp4_rule, monkeypatch, "nvfp4_block_scale", bad)
+
+
 # ---------------------------------------------------------------- end to end
 
 def test_zero_latent_gives_zero_codes_and_floor_scales():
