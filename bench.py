@@ -11,8 +11,8 @@ outside the CUDA-event intervals.  Also measured in the same run: the quantizer 
 BF16 [4632, 7168] (GB/s against HBM), the GEMM's own launch time (for the
 roofline), the end-to-end call with pinned host buffers (copies inside the
 timed region), decode steps replayed from a CUDA graph (1, 8, 32, 64
-tokens), a token sweep (128 ... 65536), and the CPU oracle on a bounded
-sample of the same workload.
+tokens), a token sweep (128 ... 65536), the step with each FP4 output
+variant, and the CPU oracle on a bounded sample of the same workload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -310,6 +310,26 @@ def run_ours(args):
                 "peak_source": f"{peak_kind} bf16 x {FP8_OVER_BF16:g} (FP8/BF16 nominal ratio)",
                 "avg_launch_ms": k2_avg_ms, "flops_per_launch": M * FLOPS_PER_TOKEN}
 
+    # ------------------------------------- FP4 output variants (prefill step)
+    # The same step with each FP4 output variant of iq_prepare_q_ex (L2
+    # flushed before every step, 50 steps each).
+    fp4_formats = {}
+    for fmt in ("mx", "mx_ocp", "nv"):
+        q_f = torch.empty((M, N_Q // 2), dtype=torch.uint8, device=dev)
+        s_f = torch.empty((M, iq.fp4_scale_bytes(fmt)), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            iq.prepare_q(lat, w, ws, p, q_fp4=q_f, q_sf=s_f, workspace=work, fp4_format=fmt)
+        fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+        for a, b in fev:
+            flush_l2()
+            a.record(stream)
+            iq.prepare_q(lat, w, ws, p, q_fp4=q_f, q_sf=s_f, workspace=work, fp4_format=fmt)
+            b.record(stream)
+        torch.cuda.synchronize()
+        f_ms = sum(a.elapsed_time(b) for a, b in fev) / len(fev)
+        fp4_formats[fmt] = {"us_per_step": f_ms * 1e3, "tokens_per_s": M / (f_ms * 1e-3),
+                            "scale_bytes_per_token": iq.fp4_scale_bytes(fmt)}
+
     # ------------------------------------------------- the quantizer alone
     xb = W.quant_blocks_input(M_PREFILL, K_QUANT, seed=1)
     X = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -508,7 +528,7 @@ def run_ours(args):
             "gpu_launches": 2 * args.steps,
             "clocks": clocks.summary(),
             "k1_chain_avg_ms": k1_avg_ms, "wall_s_timed": t_wall,
-            "decode": decode, "sweep": sweep,
+            "decode": decode, "sweep": sweep, "fp4_formats": fp4_formats,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

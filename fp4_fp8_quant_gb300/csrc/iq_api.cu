@@ -99,7 +99,7 @@ iq::RopeTurns make_rope_turns() {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq, const uint8_t* wq_sf,
-                     const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf, float* q_pre, int max_pairs,
+                     const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf, float* q_pre, int fmt, int max_pairs,
                      cudaStream_t stream) {
   static const iq::RopeTurns rope = make_rope_turns();
   iq::GemmArgs a;
@@ -124,7 +124,7 @@ iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq,
         !encode_2d_u8(&tm_w, wq, iq::kLatentDim, iq::kQDim, 128, iq::kHeadDim)) {
       return IQ_ERR_CUDA;
     }
-    return iq::launch_small_m_rope_hadamard_fp4(tm_x, tm_w, a, stream) == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
+    return iq::launch_small_m_rope_hadamard_fp4(tm_x, tm_w, a, fmt, stream) == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
   }
   // X: this CTA's 128 token rows per K-block; W: one head (128 rows) per
   // CTA of the pair; Q codes: one head of 128 rows x 64 bytes per store.
@@ -133,17 +133,19 @@ iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq,
       !encode_2d_u8(&tm_q, q_fp4, iq::kQDim / 2, static_cast<uint64_t>(M), 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) {
     return IQ_ERR_CUDA;
   }
-  return iq::launch_gemm_rope_hadamard_fp4(tm_x, tm_w, tm_q, a, max_pairs, stream) == cudaSuccess ? IQ_OK
-                                                                                                   : IQ_ERR_CUDA;
+  return iq::launch_gemm_rope_hadamard_fp4(tm_x, tm_w, tm_q, a, fmt, max_pairs, stream) == cudaSuccess ? IQ_OK
+                                                                                                        : IQ_ERR_CUDA;
 }
 
+bool valid_format(int fmt) { return fmt == IQ_FP4_MX || fmt == IQ_FP4_MX_OCP || fmt == IQ_FP4_NV; }
+
 iq_status check_prepare_args(const void* latent, int M, const void* wq, const uint8_t* wq_sf, const int32_t* pos,
-                             uint8_t* q_fp4, uint8_t* q_sf, const float* q_pre, bool need_pre) {
-  if (M < 0) return IQ_ERR_ARG;
+                             uint8_t* q_fp4, uint8_t* q_sf, const float* q_pre, bool need_pre, int fmt = IQ_FP4_MX) {
+  if (M < 0 || !valid_format(fmt)) return IQ_ERR_ARG;
   if (M == 0) return IQ_OK;
   if (!latent || !wq || !wq_sf || !pos || !q_fp4 || !q_sf || (need_pre && !q_pre)) return IQ_ERR_ARG;
-  if (!aligned(latent, 16) || !aligned(wq, 16) || !aligned(pos, 4) || !aligned(q_fp4, 16) || !aligned(q_sf, 4) ||
-      (q_pre && !aligned(q_pre, 16))) {
+  if (!aligned(latent, 16) || !aligned(wq, 16) || !aligned(pos, 4) || !aligned(q_fp4, 16) ||
+      !aligned(q_sf, fmt == IQ_FP4_NV ? 8 : 4) || (q_pre && !aligned(q_pre, 16))) {
     return IQ_ERR_ALIGN;
   }
   return IQ_OK;
@@ -151,8 +153,8 @@ iq_status check_prepare_args(const void* latent, int M, const void* wq, const ui
 
 iq_status prepare_impl(const void* latent, int M, const void* wq, const uint8_t* wq_sf, const int32_t* pos,
                        uint8_t* q_fp4, uint8_t* q_sf, float* q_pre, bool need_pre, void* ws, size_t ws_bytes,
-                       cudaStream_t stream) {
-  iq_status st = check_prepare_args(latent, M, wq, wq_sf, pos, q_fp4, q_sf, q_pre, need_pre);
+                       int fmt, cudaStream_t stream) {
+  iq_status st = check_prepare_args(latent, M, wq, wq_sf, pos, q_fp4, q_sf, q_pre, need_pre, fmt);
   if (st != IQ_OK || M == 0) return st;
   if (!ws) return IQ_ERR_ARG;
   if (!aligned(ws, 256)) return IQ_ERR_ALIGN;
@@ -166,7 +168,7 @@ iq_status prepare_impl(const void* latent, int M, const void* wq, const uint8_t*
       cudaSuccess) {
     return IQ_ERR_CUDA;
   }
-  return gemm_stage(xq, x_sf, M, wq, wq_sf, pos, q_fp4, q_sf, q_pre, max_pairs, stream);
+  return gemm_stage(xq, x_sf, M, wq, wq_sf, pos, q_fp4, q_sf, q_pre, fmt, max_pairs, stream);
 }
 
 }  // namespace
@@ -237,14 +239,30 @@ iq_status iq_prepare_q(const void* latent_bf16, int M, const void* wq_e4m3, cons
                        const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf, void* workspace, size_t ws_bytes,
                        cudaStream_t stream) {
   return prepare_impl(latent_bf16, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, nullptr, false, workspace, ws_bytes,
-                      stream);
+                      IQ_FP4_MX, stream);
 }
 
 iq_status iq_prepare_q_debug(const void* latent_bf16, int M, const void* wq_e4m3, const uint8_t* wq_sf,
                              const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf, float* q_prequant,
                              void* workspace, size_t ws_bytes, cudaStream_t stream) {
   return prepare_impl(latent_bf16, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, q_prequant, true, workspace, ws_bytes,
-                      stream);
+                      IQ_FP4_MX, stream);
+}
+
+size_t iq_fp4_scale_bytes(int fp4_format) {
+  switch (fp4_format) {
+    case IQ_FP4_MX:
+    case IQ_FP4_MX_OCP: return iq::Fp4Layout<iq::kFp4Mx>::kScaleBytesPerToken;
+    case IQ_FP4_NV: return iq::Fp4Layout<iq::kFp4Nv>::kScaleBytesPerToken;
+  }
+  return 0;
+}
+
+iq_status iq_prepare_q_ex(const void* latent_bf16, int M, const void* wq_e4m3, const uint8_t* wq_sf,
+                          const int32_t* positions, int fp4_format, uint8_t* q_fp4, uint8_t* q_sf, float* q_prequant,
+                          void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return prepare_impl(latent_bf16, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, q_prequant, false, workspace, ws_bytes,
+                      fp4_format, stream);
 }
 
 iq_status iq_gemm_rope_hadamard_fp4(const void* xq_e4m3, const int32_t* x_scales, int M, const void* wq_e4m3,
@@ -257,7 +275,8 @@ iq_status iq_gemm_rope_hadamard_fp4(const void* xq_e4m3, const int32_t* x_scales
   int max_pairs = 0;
   st = device_setup(&max_pairs);
   if (st != IQ_OK) return st;
-  return gemm_stage(xq_e4m3, x_scales, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, q_prequant, max_pairs, stream);
+  return gemm_stage(xq_e4m3, x_scales, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, q_prequant, IQ_FP4_MX, max_pairs,
+                    stream);
 }
 
 }  // extern "C"
@@ -315,5 +334,5 @@ extern "C" iq_status iq_prepare_q_static(const void* latent_bf16, int M, const v
       cudaSuccess) {
     return IQ_ERR_CUDA;
   }
-  return gemm_stage(xq, x_sf, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, nullptr, max_pairs, stream);
+  return gemm_stage(xq, x_sf, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, nullptr, IQ_FP4_MX, max_pairs, stream);
 }

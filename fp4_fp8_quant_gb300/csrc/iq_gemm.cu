@@ -107,6 +107,7 @@ __device__ __forceinline__ void fail(volatile uint32_t* abort_flag, uint32_t bit
 // `stage_row`, this row's 64 bytes of the shared staging tile, stored with the
 // 64-byte swizzle of the bulk tensor store (16-byte chunk c of row r at chunk
 // c ^ ((r >> 1) & 3)): a warp's 16-byte writes then fall on distinct banks.
+template <int kFmt>
 __device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int head, int pos, const GemmArgs& args,
                                              uint8_t* stage_row, int swz) {
   // NeoX RoPE on dims 0..63: pairs (i, i+32), angle = pos * 10000^(-i/32).
@@ -159,36 +160,68 @@ __device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int hea
       }
     }
   }
-  // FP4: z = v / sqrt(128); per 32-block scale e; codes = E2M1(z * 2^-e).
-  // z * 2^-e is formed as v * (2^-e / sqrt(128)), equal to fp32(z) * 2^-e.
+  // FP4 of z = v / sqrt(128), per block of the variant.
   uint32_t codes[16];
-  uint32_t sfw = 0;
+  if constexpr (kFmt != kFp4Nv) {
+    // MXFP4: per 32-block UE8M0 exponent e; codes = E2M1(z * 2^-e), formed
+    // as v * (2^-e / sqrt(128)), equal to fp32(z) * 2^-e.
+    uint32_t sfw = 0;
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    float amax = 0.f;
+    for (int b = 0; b < 4; ++b) {
+      float amax = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      float x0, x1;
-      f2_unpack(p[16 * b + j], x0, x1);
-      amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+      for (int j = 0; j < 16; ++j) {
+        float x0, x1;
+        f2_unpack(p[16 * b + j], x0, x1);
+        amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+      }
+      const int e = fp4_block_exponent<kFmt>(amax * kInvSqrt128);
+      const float k = fp4_code_factor(e);
+      const uint64_t kk = f2_pack(k, k);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        float q[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f2_unpack(f2_mul(p[16 * b + 4 * t + j], kk), q[2 * j], q[2 * j + 1]);
+        codes[4 * b + t] = cvt_e2m1x8(q);
+      }
+      sfw |= static_cast<uint32_t>(e + 127) << (8 * b);
     }
-    const int e = fp4_scale_exponent(amax * kInvSqrt128);
-    const float k = fp4_code_factor(e);
-    const uint64_t kk = f2_pack(k, k);
+    *reinterpret_cast<uint32_t*>(args.q_sf + static_cast<long long>(row) * Fp4Layout<kFmt>::kScaleBytesPerToken +
+                                 head * 4) = sfw;
+  } else {
+    // NVFP4-style: per 16-block E4M3 scale s; codes = E2M1(fp32(z) * fp32(1/s)).
+    const uint64_t c2 = f2_pack(kInvSqrt128, kInvSqrt128);
+    uint32_t sfw[2] = {0u, 0u};
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      float q[8];
+    for (int b = 0; b < 8; ++b) {
+      float amax = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) f2_unpack(f2_mul(p[16 * b + 4 * t + j], kk), q[2 * j], q[2 * j + 1]);
-      codes[4 * b + t] = cvt_e2m1x8(q);
+      for (int j = 0; j < 8; ++j) {
+        float x0, x1;
+        f2_unpack(p[8 * b + j], x0, x1);
+        amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+      }
+      float sv;
+      const uint32_t code = nvfp4_scale_code(amax * kInvSqrt128, &sv);
+      const float r = __frcp_rn(sv);
+      const uint64_t rr = f2_pack(r, r);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        float q[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f2_unpack(f2_mul(f2_mul(p[8 * b + 4 * t + j], c2), rr), q[2 * j], q[2 * j + 1]);
+        codes[2 * b + t] = cvt_e2m1x8(q);
+      }
+      sfw[b >> 2] |= code << (8 * (b & 3));
     }
-    sfw |= static_cast<uint32_t>(e + 127) << (8 * b);
+    *reinterpret_cast<uint2*>(args.q_sf + static_cast<long long>(row) * Fp4Layout<kFmt>::kScaleBytesPerToken +
+                              head * 8) = make_uint2(sfw[0], sfw[1]);
   }
 #pragma unroll
   for (int t = 0; t < 4; ++t)
     *reinterpret_cast<uint4*>(stage_row + ((t ^ swz) << 4)) =
         make_uint4(codes[4 * t], codes[4 * t + 1], codes[4 * t + 2], codes[4 * t + 3]);
-  *reinterpret_cast<uint32_t*>(args.q_sf + static_cast<long long>(row) * (kQDim / 32) + head * 4) = sfw;
   if (args.q_pre != nullptr) {
     const uint64_t c2 = f2_pack(kInvSqrt128, kInvSqrt128);
     float4* pre = reinterpret_cast<float4*>(args.q_pre + static_cast<long long>(row) * kQDim + head * kHeadDim);
@@ -202,6 +235,7 @@ __device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int hea
   }
 }
 
+template <int kFmt>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_rope_hadamard_fp4_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ GemmArgs args) {
@@ -487,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t p[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) p[j] = f2_pack(v[2 * j], v[2 * j + 1]);
-      if (row < args.M) epilogue_row(p, row, head, pos, args, stage_row, swz);
+      if (row < args.M) epilogue_row<kFmt>(p, row, head, pos, args, stage_row, swz);
       fence_proxy_async_smem();
       named_barrier_sync(1, kNumEpiWarps * 32);
       if (store_issuer) {
@@ -538,20 +572,28 @@ int gemm_smem_bytes() { return kSmemBytes; }
 int gemm_pair_size() { return kPair; }
 
 cudaError_t gemm_setup_device(int* max_pairs) {
-  cudaError_t err = cudaFuncSetAttribute(gemm_rope_hadamard_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
-  if (err != cudaSuccess) return err;
+  for (const void* fn : {reinterpret_cast<const void*>(gemm_rope_hadamard_fp4_kernel<kFp4Mx>),
+                         reinterpret_cast<const void*>(gemm_rope_hadamard_fp4_kernel<kFp4MxOcp>),
+                         reinterpret_cast<const void*>(gemm_rope_hadamard_fp4_kernel<kFp4Nv>)}) {
+    const cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err != cudaSuccess) return err;
+  }
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pair_config(1, attr, nullptr);
-  return cudaOccupancyMaxActiveClusters(max_pairs, gemm_rope_hadamard_fp4_kernel, &cfg);
+  return cudaOccupancyMaxActiveClusters(max_pairs, gemm_rope_hadamard_fp4_kernel<kFp4Mx>, &cfg);
 }
 
 cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
-                                          const GemmArgs& args, int max_pairs, cudaStream_t stream) {
+                                          const GemmArgs& args, int fp4_format, int max_pairs, cudaStream_t stream) {
   const int pairs = args.num_pair_tiles < max_pairs ? args.num_pair_tiles : max_pairs;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pair_config(pairs, attr, stream);
-  return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel, tm_x, tm_w, tm_q, args);
+  switch (fp4_format) {
+    case kFp4Mx: return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel<kFp4Mx>, tm_x, tm_w, tm_q, args);
+    case kFp4MxOcp: return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel<kFp4MxOcp>, tm_x, tm_w, tm_q, args);
+    case kFp4Nv: return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel<kFp4Nv>, tm_x, tm_w, tm_q, args);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t read_device_status(uint32_t* flags, bool reset) {

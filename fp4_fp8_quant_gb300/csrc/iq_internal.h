@@ -21,6 +21,22 @@ constexpr int kNumKBlocks = kLatentDim / 128; // 12
 constexpr int kScaleGroups = kNumKBlocks / 4; // 3 packed int32 words per row
 constexpr int kSmallMMax = 64;                // most tokens the small-M kernel takes
 
+// FP4 output variants (compile-time parameter of the fused GEMM kernels).
+//   kFp4Mx:    1x32 blocks, UE8M0 scale 2^e with e the smallest integer with
+//              6 * 2^e >= amax (never saturates);
+//   kFp4MxOcp: 1x32 blocks, UE8M0 scale 2^(floor(log2 amax) - 2) (OCP MX rule,
+//              elements saturate at 6);
+//   kFp4Nv:    1x16 blocks, E4M3 scale = round-to-nearest of amax / 6 (2^-9 if
+//              that is zero), codes of z * (1 / scale).
+enum Fp4Format : int { kFp4Mx = 0, kFp4MxOcp = 1, kFp4Nv = 2 };
+
+template <int kFmt>
+struct Fp4Layout {
+  static constexpr int kBlock = kFmt == kFp4Nv ? 16 : 32;   // elements per scale
+  static constexpr int kBlocksPerHead = kHeadDim / kBlock;  // scale bytes per (token, head)
+  static constexpr int kScaleBytesPerToken = kQDim / kBlock;
+};
+
 // RoPE frequencies of the 32 NeoX pairs, in turns per position unit:
 // 10000^(-i/32) / (2 pi), split into a float32 head and tail.
 struct RopeTurns {
@@ -33,7 +49,7 @@ struct GemmArgs {
   const uint8_t* w_sf;   // [64][12] UE8M0 bytes of the weight blocks
   const int32_t* pos;    // [M]
   uint8_t* q_fp4;        // [M][4096]
-  uint8_t* q_sf;         // [M][256]
+  uint8_t* q_sf;         // [M][Fp4Layout<format>::kScaleBytesPerToken]
   float* q_pre;          // [M][8192] or nullptr
   int M;
   int m_al;
@@ -62,13 +78,13 @@ int gemm_smem_bytes();
 int gemm_pair_size();
 
 cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
-                                          const GemmArgs& args, int max_pairs, cudaStream_t stream);
+                                          const GemmArgs& args, int fp4_format, int max_pairs, cudaStream_t stream);
 
 // The small-M (swapped-operand) kernel: M <= kSmallMMax tokens, one launch
 // of 64 clusters of two CTAs (one per K half).
 cudaError_t small_m_setup_device();
 cudaError_t launch_small_m_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const GemmArgs& args,
-                                             cudaStream_t stream);
+                                             int fp4_format, cudaStream_t stream);
 
 // Device status words of the large-M and small-M kernels (synchronous).
 cudaError_t read_device_status(uint32_t* flags, bool reset);

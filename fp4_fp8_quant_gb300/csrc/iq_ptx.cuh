@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 namespace iq {
 
@@ -382,6 +383,14 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Value of an E4M3 code (exact: every E4M3 value is a half).
+__device__ __forceinline__ float e4m3_to_float(uint32_t code) {
+  uint32_t h2;
+  const uint16_t c = static_cast<uint16_t>(code & 0xFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
 }
 
 // Eight floats -> eight E2M1 codes (RNE, saturating) in one word: element i in

@@ -109,6 +109,7 @@ __device__ __forceinline__ void fail(volatile uint32_t* abort_flag, uint32_t bit
   *abort_flag = 1u;
 }
 
+template <int kFmt>
 __global__ void __launch_bounds__(kThreads, 1)
     small_m_rope_hadamard_fp4_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                                      const __grid_constant__ GemmArgs args) {
@@ -403,13 +404,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // FP4: block b of 32 dims = lanes 8b..8b+7; z = v / sqrt(128).
+    // FP4 of z = v / sqrt(128): a block of 32 dims is lanes 8b..8b+7 (MX
+    // variants), a block of 16 dims lanes 4b..4b+3 (NVFP4-style).
+    constexpr int kLanesPerBlock = Fp4Layout<kFmt>::kBlock / 4;
     float amax[kTokPerWarp];
 #pragma unroll
     for (int j = 0; j < kTokPerWarp; ++j)
       amax[j] = fmaxf(fmaxf(fabsf(x[j][0]), fabsf(x[j][1])), fmaxf(fabsf(x[j][2]), fabsf(x[j][3])));
 #pragma unroll
-    for (int m = 1; m < 8; m <<= 1) {
+    for (int m = 1; m < kLanesPerBlock; m <<= 1) {
 #pragma unroll
       for (int j = 0; j < kTokPerWarp; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], m));
     }
@@ -417,12 +420,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < kTokPerWarp; ++j) {
       if (!tok_valid[j]) continue;   // warp-uniform
       const long long t = tok_index[j];
-      const int e = fp4_scale_exponent(amax[j] * kInvSqrt128);
-      const float kq = fp4_code_factor(e);
-      const uint32_t codes = cvt_e2m1x4(x[j][0] * kq, x[j][1] * kq, x[j][2] * kq, x[j][3] * kq);
+      uint32_t codes, sbyte;
+      if constexpr (kFmt != kFp4Nv) {
+        const int e = fp4_block_exponent<kFmt>(amax[j] * kInvSqrt128);
+        const float kq = fp4_code_factor(e);
+        codes = cvt_e2m1x4(x[j][0] * kq, x[j][1] * kq, x[j][2] * kq, x[j][3] * kq);
+        sbyte = static_cast<uint32_t>(e + 127);
+      } else {
+        float sv;
+        sbyte = nvfp4_scale_code(amax[j] * kInvSqrt128, &sv);
+        const float r = __frcp_rn(sv);
+        codes = cvt_e2m1x4(__fmul_rn(__fmul_rn(x[j][0], kInvSqrt128), r), __fmul_rn(__fmul_rn(x[j][1], kInvSqrt128), r),
+                           __fmul_rn(__fmul_rn(x[j][2], kInvSqrt128), r), __fmul_rn(__fmul_rn(x[j][3], kInvSqrt128), r));
+      }
       // Byte 64 h + 2 l + i of the token's row holds dims 4l + 2i, 4l + 2i + 1.
       reinterpret_cast<uint16_t*>(args.q_fp4 + t * (kQDim / 2) + head * 64)[lane] = static_cast<uint16_t>(codes);
-      if ((lane & 7) == 0) args.q_sf[t * (kQDim / 32) + head * 4 + (lane >> 3)] = static_cast<uint8_t>(e + 127);
+      if (lane % kLanesPerBlock == 0)
+        args.q_sf[t * Fp4Layout<kFmt>::kScaleBytesPerToken + head * Fp4Layout<kFmt>::kBlocksPerHead +
+                  lane / kLanesPerBlock] = static_cast<uint8_t>(sbyte);
       if (args.q_pre != nullptr) {
         reinterpret_cast<float4*>(args.q_pre + t * kQDim + head * kHeadDim)[lane] =
             make_float4(x[j][0] * kInvSqrt128, x[j][1] * kInvSqrt128, x[j][2] * kInvSqrt128, x[j][3] * kInvSqrt128);
@@ -456,15 +471,25 @@ cudaLaunchConfig_t small_m_config(cudaLaunchAttribute* attr, cudaStream_t stream
 }  // namespace
 
 cudaError_t small_m_setup_device() {
-  return cudaFuncSetAttribute(small_m_rope_hadamard_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemBytes);
+  for (const void* fn : {reinterpret_cast<const void*>(small_m_rope_hadamard_fp4_kernel<kFp4Mx>),
+                         reinterpret_cast<const void*>(small_m_rope_hadamard_fp4_kernel<kFp4MxOcp>),
+                         reinterpret_cast<const void*>(small_m_rope_hadamard_fp4_kernel<kFp4Nv>)}) {
+    const cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_small_m_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const GemmArgs& args,
-                                             cudaStream_t stream) {
+                                             int fp4_format, cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = small_m_config(attr, stream);
-  return cudaLaunchKernelEx(&cfg, small_m_rope_hadamard_fp4_kernel, tm_x, tm_w, args);
+  switch (fp4_format) {
+    case kFp4Mx: return cudaLaunchKernelEx(&cfg, small_m_rope_hadamard_fp4_kernel<kFp4Mx>, tm_x, tm_w, args);
+    case kFp4MxOcp: return cudaLaunchKernelEx(&cfg, small_m_rope_hadamard_fp4_kernel<kFp4MxOcp>, tm_x, tm_w, args);
+    case kFp4Nv: return cudaLaunchKernelEx(&cfg, small_m_rope_hadamard_fp4_kernel<kFp4Nv>, tm_x, tm_w, args);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t read_small_m_status(uint32_t* flags, bool reset) {

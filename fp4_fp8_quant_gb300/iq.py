@@ -40,7 +40,12 @@ SIGNATURES = {
     "iq_prepare_q_static": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
     "iq_set_small_m_threshold": (_I, [_I]),
     "iq_small_m_threshold": (_I, []),
+    "iq_fp4_scale_bytes": (_SZ, [_I]),
+    "iq_prepare_q_ex": (_I, [_P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
 }
+
+# FP4 output variants (include/iq.h, iq_fp4_format).
+FP4_FORMATS = {"mx": 0, "mx_ocp": 1, "nv": 2}
 
 _lib = None
 
@@ -131,34 +136,51 @@ def prepare_q_workspace_bytes(M: int) -> int:
     return int(lib().iq_prepare_q_workspace(M))
 
 
-def _prepare_out(M, device, q_fp4, q_sf):
+def fp4_scale_bytes(fp4_format: str = "mx") -> int:
+    """Scale bytes per token of an FP4 output variant (256 or 512)."""
+    return int(lib().iq_fp4_scale_bytes(FP4_FORMATS[fp4_format]))
+
+
+def _prepare_out(M, device, q_fp4, q_sf, fp4_format="mx"):
+    sf_cols = Q_DIM // 16 if fp4_format == "nv" else Q_DIM // 32
     if q_fp4 is None:
         q_fp4 = torch.empty((M, Q_DIM // 2), dtype=torch.uint8, device=device)
     if q_sf is None:
-        q_sf = torch.empty((M, Q_DIM // 32), dtype=torch.uint8, device=device)
+        q_sf = torch.empty((M, sf_cols), dtype=torch.uint8, device=device)
     _require(q_fp4, "q_fp4", (torch.uint8,), (M, Q_DIM // 2))
-    _require(q_sf, "q_sf", (torch.uint8,), (M, Q_DIM // 32))
+    _require(q_sf, "q_sf", (torch.uint8,), (M, sf_cols))
     return q_fp4, q_sf
 
 
 def prepare_q(latent: torch.Tensor, wq: torch.Tensor, wq_sf: torch.Tensor, positions: torch.Tensor, *,
               q_fp4: torch.Tensor | None = None, q_sf: torch.Tensor | None = None,
               workspace: torch.Tensor | None = None, q_prequant: torch.Tensor | None = None,
-              debug: bool = False, stream=None):
+              debug: bool = False, fp4_format: str = "mx", stream=None):
     """Indexer-Q preparation: returns (q_fp4 uint8 [M, 4096], q_sf uint8
-    [M, 256]) and, with debug=True, also the float32 pre-quant Q [M, 8192]."""
+    [M, 256] ([M, 512] for fp4_format="nv")) and, with debug=True, also the
+    float32 pre-quant Q [M, 8192].  fp4_format: "mx" (default), "mx_ocp" or
+    "nv" (include/iq.h, FP4 output variants)."""
     M = latent.shape[0]
+    if fp4_format not in FP4_FORMATS:
+        raise ValueError(f"fp4_format must be one of {sorted(FP4_FORMATS)}")
     _require(latent, "latent", (torch.bfloat16,), (M, LATENT_DIM))
     _require(wq, "wq", _U8, (Q_DIM, LATENT_DIM))
     _require(wq_sf, "wq_sf", (torch.uint8,), (N_HEADS, LATENT_DIM // 128))
     _require(positions, "positions", (torch.int32,), (M,))
-    q_fp4, q_sf = _prepare_out(M, latent.device, q_fp4, q_sf)
+    q_fp4, q_sf = _prepare_out(M, latent.device, q_fp4, q_sf, fp4_format)
     ws_bytes = prepare_q_workspace_bytes(M)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=latent.device)
     _require(workspace, "workspace", (torch.uint8,))
     if debug and q_prequant is None:
         q_prequant = torch.empty((M, Q_DIM), dtype=torch.float32, device=latent.device)
+    if fp4_format != "mx":
+        if q_prequant is not None:
+            _require(q_prequant, "q_prequant", (torch.float32,), (M, Q_DIM))
+        _check(lib().iq_prepare_q_ex(_ptr(latent), M, _ptr(wq), _ptr(wq_sf), _ptr(positions),
+                                     FP4_FORMATS[fp4_format], _ptr(q_fp4), _ptr(q_sf), _ptr(q_prequant),
+                                     _ptr(workspace), workspace.numel(), _stream(stream)), "iq_prepare_q_ex")
+        return (q_fp4, q_sf, q_prequant) if q_prequant is not None else (q_fp4, q_sf)
     if q_prequant is not None:
         _require(q_prequant, "q_prequant", (torch.float32,), (M, Q_DIM))
         _check(lib().iq_prepare_q_debug(_ptr(latent), M, _ptr(wq), _ptr(wq_sf), _ptr(positions), _ptr(q_fp4),

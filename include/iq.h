@@ -200,6 +200,40 @@ iq_status iq_gemm_rope_hadamard_fp4(const void* xq_e4m3, const int32_t* x_scales
                                     cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * FP4 output variants.  iq_prepare_q writes MXFP4 with the scale rule above
+ * (IQ_FP4_MX).  iq_prepare_q_ex selects one of:
+ *   IQ_FP4_MX      1x32 blocks, UE8M0 scale 2^e, e the smallest integer with
+ *                  6 * 2^e >= max(amax, 1e-4); never saturates.  q_sf [M, 256].
+ *   IQ_FP4_MX_OCP  1x32 blocks, UE8M0 scale 2^e with e = floor(log2(max(amax,
+ *                  1e-4))) - 2, the shared-scale rule of the OCP Microscaling
+ *                  (MX) spec for E2M1; elements saturate at 6.  q_sf [M, 256].
+ *   IQ_FP4_NV      1x16 blocks with an E4M3 scale s (NVFP4-style, per-tensor
+ *                  scale 1): s = round-to-nearest-even E4M3 of
+ *                  float32(max(amax, 1e-4) / 6), or 2^-9 (code 1) when that
+ *                  rounds to zero; codes E2M1(float32(z * float32(1 / s))),
+ *                  saturating at 6.  q_sf [M, 512] E4M3 bytes, byte 8 h + b the
+ *                  scale of block b (dims 16 b .. 16 b + 15) of head h; 8-byte
+ *                  aligned.
+ * The pages specify only the MXFP4 output; the other two are variants of the
+ * same FP4 stage for consumers that expect them.
+ * ------------------------------------------------------------------------ */
+
+typedef enum { IQ_FP4_MX = 0, IQ_FP4_MX_OCP = 1, IQ_FP4_NV = 2 } iq_fp4_format;
+
+/* Scale bytes per token of a format (256 or 512); 0 for an unknown format. */
+size_t iq_fp4_scale_bytes(int fp4_format);
+
+/* iq_prepare_q with the FP4 output variant `fp4_format` (iq_fp4_format);
+ * q_sf holds iq_fp4_scale_bytes(fp4_format) bytes per token; q_prequant may
+ * be NULL, else it receives the float32 pre-quant Q as in iq_prepare_q_debug.
+ * An unknown format returns IQ_ERR_ARG. */
+iq_status iq_prepare_q_ex(const void* latent_bf16, int M,
+                          const void* wq_e4m3, const uint8_t* wq_sf,
+                          const int32_t* positions, int fp4_format,
+                          uint8_t* q_fp4, uint8_t* q_sf, float* q_prequant,
+                          void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Indexer-Q preparation without any device allocation.  The pages have no
  * counterpart of this call; it exists for callers that cannot obtain device
  * memory at the point where they prepare Q -- for example a plugin whose host

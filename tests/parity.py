@@ -6,10 +6,13 @@
 * FP4 output: the FP4 decisions of both sides are taken on float32 values that
   differ by the GPU's float32 rounding, so they may differ only where the
   oracle's value sits next to a decision boundary:
-    - a block's scale byte may differ only where the oracle's floored amax / 6
-      is within 1e-4 relative of a power of two; such blocks are compared by
-      decoded value (within one step of the finer of the two scales) and all
-      their elements count as mismatches;
+    - a block's scale byte may differ only next to the scale rule's decision
+      boundary, within 1e-4 relative of it: the oracle's floored amax / 6 at a
+      power of two (MXFP4, ceil rule), amax at a power of two (MXFP4, OCP
+      floor rule), amax / 6 at a rounding midpoint between two E4M3 values
+      (NVFP4-style); in such blocks the GPU's codes must be a correct rounding
+      of the values under the GPU's own scale (same one-step rule as below)
+      and all their elements count as mismatches;
     - in blocks with equal scales, a code may differ only by one step on the
       E2M1 grid, at an oracle value u = z * 2^-e within 1e-4 relative of the
       rounding midpoint between the two codes; a sign difference of a value
@@ -62,65 +65,87 @@ def _code_index(c):
     return (c & 0x7).astype(np.int64)
 
 
-def check_fp4(gpu_q, gpu_sf, ora_q, ora_sf, ora_z, min_equal=0.9999):
+_E4M3_POS = O.e4m3_value_table()[:0x7F]
+_E4M3_MID = (_E4M3_POS[:-1] + _E4M3_POS[1:]) / 2
+
+
+def _units(z32, sf, fmt):
+    """The value each code encodes in units of its block's scale, computed the
+    way the format's rule does (float32 for the NVFP4 product)."""
+    if fmt == "nv":
+        s = O.decode_e4m3(sf)
+        r = (1.0 / s).astype(np.float32)
+        return (z32.astype(np.float32) * r[..., None]).astype(np.float32).astype(np.float64), s
+    e = sf.astype(np.int64) - 127
+    return z32 * np.ldexp(1.0, -e)[..., None], np.ldexp(1.0, e)
+
+
+def _near_scale_boundary(amax, fmt):
+    if fmt == "mx":          # ceil rule: amax / 6 at a power of two
+        r = amax / 6.0
+        pw = np.ldexp(1.0, np.round(np.log2(np.maximum(r, 1e-300))).astype(np.int64))
+        return np.abs(r - pw) <= 1e-4 * pw
+    if fmt == "mx_ocp":      # floor rule: amax at a power of two
+        pw = np.ldexp(1.0, np.round(np.log2(np.maximum(amax, 1e-300))).astype(np.int64))
+        return np.abs(amax - pw) <= 1e-4 * pw
+    r = amax / 6.0           # nv: amax / 6 at an E4M3 rounding midpoint
+    i = np.clip(np.searchsorted(_E4M3_MID, r), 1, len(_E4M3_MID) - 1)
+    d = np.minimum(np.abs(r - _E4M3_MID[i - 1]), np.abs(r - _E4M3_MID[i]))
+    return d <= 1e-4 * np.maximum(r, 1e-300)
+
+
+def _check_codes(gc, oc, u, mask):
+    """Codes that differ (where mask) must be one E2M1 step apart at a value
+    within 1e-4 relative of the rounding midpoint, or a sign flip of a value
+    that rounds to zero (|u| <= 6e-4).  Returns (mismatches, zero flips, worst)."""
+    diff = (gc != oc) & mask
+    if not diff.any():
+        return 0, 0, 0.0
+    idx = np.nonzero(diff)
+    g, o, uu = gc[idx], oc[idx], u[idx]
+    gi, oi = _code_index(g), _code_index(o)
+    same_sign = (g >> 3) == (o >> 3)
+    step_ok = same_sign & (np.abs(gi - oi) == 1)
+    zero_flip = (~same_sign) & (gi == 0) & (oi == 0)
+    assert np.all(step_ok | zero_flip), "FP4 code differs by more than one step"
+    lo = np.minimum(gi, oi)
+    mid = np.where(step_ok, (E2M1_GRID[lo] + E2M1_GRID[np.minimum(lo + 1, 7)]) / 2, 0.0)
+    dist = np.where(step_ok, np.abs(np.abs(uu) - mid) / np.maximum(mid, 1e-300), np.abs(uu) / 6.0)
+    worst = float(dist.max())
+    assert np.all(dist <= 1e-4), f"FP4 code mismatch {worst:.3g} away from a rounding boundary"
+    nz = int(zero_flip.sum())
+    return int(diff.sum()) - nz, nz, worst
+
+
+def check_fp4(gpu_q, gpu_sf, ora_q, ora_sf, ora_z, min_equal=0.9999, fmt="mx"):
     """Returns a dict of mismatch statistics; raises AssertionError on a
-    violation of the rules in the module docstring."""
+    violation of the rules in the module docstring.  fmt: the FP4 output
+    variant ("mx", "mx_ocp" or "nv"); the scale-decision boundary is the one
+    of that variant's rule."""
     gpu_q = np.asarray(gpu_q)
     gpu_sf = np.asarray(gpu_sf)
     M = ora_z.shape[0]
     assert gpu_q.shape == ora_q.shape and gpu_sf.shape == ora_sf.shape
-    gc = unpack_fp4(gpu_q).reshape(M, -1, 32)
-    oc = unpack_fp4(ora_q).reshape(M, -1, 32)
-    z32 = ora_z.astype(np.float32).astype(np.float64).reshape(M, -1, 32)
+    blk = O.NVFP4_BLOCK if fmt == "nv" else O.FP4_BLOCK
+    gc = unpack_fp4(gpu_q).reshape(M, -1, blk)
+    oc = unpack_fp4(ora_q).reshape(M, -1, blk)
+    z32 = ora_z.astype(np.float32).astype(np.float64).reshape(M, -1, blk)
     amax = np.maximum(np.abs(z32).max(axis=2), O.AMAX_FLOOR)
 
-    # scale bytes
+    # scale bytes: may differ only next to the variant's decision boundary;
+    # there the GPU's codes must be a correct rounding under its own scale
     sf_diff = gpu_sf != ora_sf
-    e_o = ora_sf.astype(np.int64) - 127
-    e_g = gpu_sf.astype(np.int64) - 127
-    near_pow2 = np.zeros_like(sf_diff)
-    r = amax / 6.0
-    pw = np.ldexp(1.0, np.round(np.log2(r)).astype(np.int64))
-    near_pow2 = np.abs(r - pw) <= 1e-4 * pw
-    bad_sf = sf_diff & ~near_pow2
-    assert not bad_sf.any(), f"{int(bad_sf.sum())} FP4 scale bytes differ away from a power-of-two boundary, " \
+    bad_sf = sf_diff & ~_near_scale_boundary(amax, fmt)
+    assert not bad_sf.any(), f"{int(bad_sf.sum())} FP4 scale bytes differ away from a decision boundary, " \
                              f"first {np.argwhere(bad_sf)[:5].tolist()}"
-    n_mis = 0
+    n_mis = int(sf_diff.sum()) * blk
     if sf_diff.any():
-        idx = np.argwhere(sf_diff)
-        for m, b in idx:
-            dg = O.decode_e2m1(gc[m, b]) * np.ldexp(1.0, e_g[m, b])
-            do = O.decode_e2m1(oc[m, b]) * np.ldexp(1.0, e_o[m, b])
-            ef = min(e_g[m, b], e_o[m, b])
-            u = np.abs(z32[m, b]) * np.ldexp(1.0, -ef)
-            step = np.where(u < 2, 0.5, np.where(u < 4, 1.0, 2.0)) * np.ldexp(1.0, ef)
-            assert np.all(np.abs(dg - do) <= step + 1e-300), f"block ({m},{b}) decoded values too far apart"
-        n_mis += int(sf_diff.sum()) * 32
+        u_g, _ = _units(z32, gpu_sf, fmt)
+        _check_codes(gc, O.round_to_e2m1_codes(u_g), u_g, np.broadcast_to(sf_diff[..., None], gc.shape))
 
     # codes in blocks whose scales agree
-    same = ~sf_diff
-    diff = (gc != oc) & same[..., None]
-    n_code = int(diff.sum())
-    n_zero_flip = 0
-    worst_rel = 0.0
-    if n_code:
-        mi, bi, ji = np.nonzero(diff)
-        g = gc[mi, bi, ji]
-        o = oc[mi, bi, ji]
-        u = z32[mi, bi, ji] * np.ldexp(1.0, -e_o[mi, bi])
-        gi, oi = _code_index(g), _code_index(o)
-        gs, os_ = g >> 3, o >> 3
-        same_sign = gs == os_
-        step_ok = same_sign & (np.abs(gi - oi) == 1)
-        zero_flip = (~same_sign) & (gi == 0) & (oi == 0)
-        assert np.all(step_ok | zero_flip), "FP4 code differs by more than one step"
-        lo = np.minimum(gi, oi)
-        mid = np.where(step_ok, (E2M1_GRID[lo] + E2M1_GRID[np.minimum(lo + 1, 7)]) / 2, 0.0)
-        dist = np.where(step_ok, np.abs(np.abs(u) - mid) / np.maximum(mid, 1e-300), np.abs(u) / 6.0)
-        worst_rel = float(dist.max())
-        assert np.all(dist <= 1e-4), f"FP4 code mismatch {worst_rel:.3g} away from a rounding boundary"
-        n_zero_flip = int(zero_flip.sum())
-        n_code -= int(zero_flip.sum())
+    u, _ = _units(z32, ora_sf, fmt)
+    n_code, n_zero_flip, worst_rel = _check_codes(gc, oc, u, np.broadcast_to(~sf_diff[..., None], gc.shape))
     n_mis += n_code
     total = gc.size
     frac_equal = 1.0 - n_mis / max(total, 1)

@@ -96,3 +96,13 @@ def test_small_m_threshold_is_clamped_and_restored(lib):
     finally:
         lib.iq_set_small_m_threshold(old)
     assert lib.iq_small_m_threshold() == old
+
+
+def test_fp4_format_helpers_and_checks(lib):
+    assert lib.iq_fp4_scale_bytes(0) == 256 and lib.iq_fp4_scale_bytes(1) == 256
+    assert lib.iq_fp4_scale_bytes(2) == 512 and lib.iq_fp4_scale_bytes(3) == 0
+    # unknown format, before anything else
+    assert lib.iq_prepare_q_ex(16, 4, 16, 16, 16, 7, 16, 16, None, 256, 1 << 20, None) == -1
+    # NVFP4 scales need 8-byte alignment
+    assert lib.iq_prepare_q_ex(16, 4, 16, 16, 16, 2, 16, 20, None, 256, 1 << 20, None) == -2
+    assert lib.iq_prepare_q_ex(16, 0, 16, 16, 16, 2, 16, 20, None, None, 0, None) == 0
