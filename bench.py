@@ -130,6 +130,14 @@ class ClockSampler:
                  "-lms", "20"], stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return self
+        # nvidia-smi takes up to a second to start (driver queries); wait for
+        # its first sample so that the start-up falls outside the timed region.
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 5.0 and self.proc.poll() is None:
+            if os.path.getsize(self.file.name) > 0:
+                break
+            time.sleep(0.01)
         return self
 
     def __exit__(self, *exc):

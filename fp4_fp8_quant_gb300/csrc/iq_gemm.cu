@@ -190,30 +190,44 @@ __device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int hea
     *reinterpret_cast<uint32_t*>(args.q_sf + static_cast<long long>(row) * Fp4Layout<kFmt>::kScaleBytesPerToken +
                                  head * 4) = sfw;
   } else {
-    // NVFP4-style: per 16-block E4M3 scale s; codes = E2M1(fp32(z) * fp32(1/s)).
+    // NVFP4-style: per 16-block E4M3 scale s = E4M3(max(amax_z, 1e-4) / 6);
+    // codes = E2M1(v * (1/s) / sqrt(128)).  Two blocks at a time in packed
+    // arithmetic; the reciprocal comes from the scale's code (no division).
     const uint64_t c2 = f2_pack(kInvSqrt128, kInvSqrt128);
+    const uint64_t sixth = f2_pack(kSixth, kSixth);
     uint32_t sfw[2] = {0u, 0u};
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      float amax = 0.f;
+    for (int b = 0; b < 8; b += 2) {
+      float am[2] = {0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float x0, x1;
-        f2_unpack(p[8 * b + j], x0, x1);
-        amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float x0, x1;
+          f2_unpack(p[8 * (b + h) + j], x0, x1);
+          am[h] = fmaxf(am[h], fmaxf(fabsf(x0), fabsf(x1)));
+        }
       }
-      float sv;
-      const uint32_t code = nvfp4_scale_code(amax * kInvSqrt128, &sv);
-      const float r = __frcp_rn(sv);
-      const uint64_t rr = f2_pack(r, r);
+      float z0, z1;
+      f2_unpack(f2_mul(f2_pack(am[0], am[1]), c2), z0, z1);
+      float t0, t1;
+      f2_unpack(f2_mul(f2_pack(fmaxf(z0, kAmaxFloor), fmaxf(z1, kAmaxFloor)), sixth), t0, t1);
+      const uint32_t code0 = nvfp4_code(t0), code1 = nvfp4_code(t1);
+      float k0, k1;
+      f2_unpack(f2_mul(f2_pack(e4m3_reciprocal(code0), e4m3_reciprocal(code1)), c2), k0, k1);
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        float q[8];
+      for (int h = 0; h < 2; ++h) {
+        const float kh = h == 0 ? k0 : k1;
+        const uint64_t kk = f2_pack(kh, kh);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) f2_unpack(f2_mul(f2_mul(p[8 * b + 4 * t + j], c2), rr), q[2 * j], q[2 * j + 1]);
-        codes[2 * b + t] = cvt_e2m1x8(q);
+        for (int t = 0; t < 2; ++t) {
+          float q[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) f2_unpack(f2_mul(p[8 * (b + h) + 4 * t + j], kk), q[2 * j], q[2 * j + 1]);
+          codes[2 * (b + h) + t] = cvt_e2m1x8(q);
+        }
       }
-      sfw[b >> 2] |= code << (8 * (b & 3));
+      sfw[b >> 2] |= (code0 | (code1 << 8)) << (8 * (b & 3));
     }
     *reinterpret_cast<uint2*>(args.q_sf + static_cast<long long>(row) * Fp4Layout<kFmt>::kScaleBytesPerToken +
                               head * 8) = make_uint2(sfw[0], sfw[1]);

@@ -427,11 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         codes = cvt_e2m1x4(x[j][0] * kq, x[j][1] * kq, x[j][2] * kq, x[j][3] * kq);
         sbyte = static_cast<uint32_t>(e + 127);
       } else {
-        float sv;
-        sbyte = nvfp4_scale_code(amax[j] * kInvSqrt128, &sv);
-        const float r = __frcp_rn(sv);
-        codes = cvt_e2m1x4(__fmul_rn(__fmul_rn(x[j][0], kInvSqrt128), r), __fmul_rn(__fmul_rn(x[j][1], kInvSqrt128), r),
-                           __fmul_rn(__fmul_rn(x[j][2], kInvSqrt128), r), __fmul_rn(__fmul_rn(x[j][3], kInvSqrt128), r));
+        sbyte = nvfp4_code(fmaxf(amax[j] * kInvSqrt128, kAmaxFloor) * kSixth);
+        const float kq = e4m3_reciprocal(sbyte) * kInvSqrt128;
+        codes = cvt_e2m1x4(x[j][0] * kq, x[j][1] * kq, x[j][2] * kq, x[j][3] * kq);
       }
       // Byte 64 h + 2 l + i of the token's row holds dims 4l + 2i, 4l + 2i + 1.
       reinterpret_cast<uint16_t*>(args.q_fp4 + t * (kQDim / 2) + head * 64)[lane] = static_cast<uint16_t>(codes);
