@@ -93,9 +93,20 @@ def load_peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def sources_sha(paths) -> str:
+    """First 16 hex digits of the SHA-256 of the listed files, concatenated in
+    order (a kernel's .cu file and every header it is compiled from)."""
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def kernel_traffic(kernel_key: str):
     """DRAM bytes per launch of a kernel from the committed ncu summary, or None
-    when the kernel's source changed since the counters were taken."""
+    when any file the kernel is compiled from changed since the counters were
+    taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -103,8 +114,9 @@ def kernel_traffic(kernel_key: str):
         t = json.load(f).get(kernel_key)
     if not t:
         return None
-    src = os.path.join(ROOT, t["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != t["source_sha"]:
+    if not all(os.path.exists(os.path.join(ROOT, rel)) for rel in t["sources"]):
+        return None
+    if sources_sha(t["sources"]) != t["sources_sha"]:
         return None
     return t["dram_bytes_per_launch"]
 
