@@ -24,6 +24,7 @@ struct DeviceInfo {
   bool ready = false;
   iq_status status = IQ_OK;
   int max_pairs = 0;   // co-resident CTA pairs of the fused GEMM kernel
+  int sm_count = 0;
 };
 
 std::mutex g_setup_mutex;
@@ -36,7 +37,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // First call on a device: check the architecture, set kernel attributes and
 // resolve the driver's tensor-map encoder.  Later calls only read the cache.
-iq_status device_setup(int* max_pairs) {
+iq_status device_setup(int* max_pairs, int* sm_count = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return IQ_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
@@ -49,6 +50,8 @@ iq_status device_setup(int* max_pairs) {
     }
     if (major != 10 || minor != 3) {
       d.status = IQ_ERR_ARCH;
+    } else if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      d.status = IQ_ERR_CUDA;
     } else if (iq::gemm_setup_device(&d.max_pairs) != cudaSuccess || d.max_pairs < 1 ||
                iq::small_m_setup_device() != cudaSuccess) {
       d.status = IQ_ERR_CUDA;
@@ -69,6 +72,7 @@ iq_status device_setup(int* max_pairs) {
     d.ready = true;
   }
   *max_pairs = d.max_pairs;
+  if (sm_count) *sm_count = d.sm_count;
   return d.status;
 }
 
@@ -335,4 +339,176 @@ extern "C" iq_status iq_prepare_q_static(const void* latent_bf16, int M, const v
     return IQ_ERR_CUDA;
   }
   return gemm_stage(xq, x_sf, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, nullptr, IQ_FP4_MX, max_pairs, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Host-buffer entry: row chunks pipelined over the host link.  Three internal
+// streams per device: `in` runs the quantizer of chunk c, which reads the
+// chunk's latent rows and positions straight from page-locked host memory;
+// `comp` (highest priority) runs the GEMM of chunk c once its quantizer is
+// done; `out` copies chunk c's FP4 codes and scales to the host once its GEMM
+// is done.  Chunk c + 1's quantizer therefore runs beside chunk c's GEMM (one
+// block per SM next to the GEMM's CTA) while chunk c - 1's results travel
+// back, and the link carries both directions at once.
+
+namespace {
+
+constexpr int kHostChunkAlign = 256;      // chunk starts stay on CTA-pair tile boundaries
+constexpr int kMaxHostChunks = 64;
+constexpr int kDefaultHostChunkRows = 1024;
+std::atomic<int> g_host_chunk_rows{kDefaultHostChunkRows};
+
+struct HostPath {
+  std::mutex mu;                          // one call at a time enqueues on the internal streams
+  bool ready = false;
+  iq_status status = IQ_OK;
+  cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
+  cudaEvent_t fork = nullptr, tail_in = nullptr, tail_comp = nullptr, join = nullptr;
+  cudaEvent_t in_done[kMaxHostChunks] = {};
+  cudaEvent_t comp_done[kMaxHostChunks] = {};
+};
+HostPath g_host[kMaxDevices];
+
+// Streams and events of the host-buffer entry on the current device, created
+// by its first call there (with the device's lock held).
+iq_status host_path_setup(HostPath& h) {
+  if (h.ready) return h.status;
+  h.ready = true;
+  int least = 0, greatest = 0;
+  const unsigned ev = cudaEventDisableTiming;
+  bool ok = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess &&
+            cudaStreamCreateWithPriority(&h.comp, cudaStreamNonBlocking, greatest) == cudaSuccess &&
+            cudaStreamCreateWithPriority(&h.in, cudaStreamNonBlocking, least) == cudaSuccess &&
+            cudaStreamCreateWithPriority(&h.out, cudaStreamNonBlocking, least) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h.fork, ev) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h.tail_in, ev) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h.tail_comp, ev) == cudaSuccess &&
+            cudaEventCreateWithFlags(&h.join, ev) == cudaSuccess;
+  for (int i = 0; ok && i < kMaxHostChunks; ++i) {
+    ok = cudaEventCreateWithFlags(&h.in_done[i], ev) == cudaSuccess &&
+         cudaEventCreateWithFlags(&h.comp_done[i], ev) == cudaSuccess;
+  }
+  h.status = ok ? IQ_OK : IQ_ERR_CUDA;
+  return h.status;
+}
+
+// The address at which kernels on device `dev` reach a caller buffer that is
+// page-locked host memory, or device / managed memory of that device; nullptr
+// for pageable host memory or another device's memory.
+const void* device_view(const void* p, int dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  switch (a.type) {
+    case cudaMemoryTypeHost:
+      return a.devicePointer;
+    case cudaMemoryTypeDevice:
+      return a.device == dev ? p : nullptr;
+    case cudaMemoryTypeManaged:
+      return p;
+    default:
+      return nullptr;
+  }
+}
+
+// Device workspace of the host-buffer entry: FP4 codes, FP4 scales and
+// positions of all M rows, then the FP8 latent and its packed scales.  Chunk
+// starts are multiples of 256 rows, so every chunk's packed-scale array
+// (3 groups x align4(rows) words) starts 3 * (first row) words in.
+size_t host_ws_bytes(int M, size_t sfb) {
+  const size_t m = static_cast<size_t>(M);
+  return align_up(m * (iq::kQDim / 2), 256) + align_up(m * sfb, 256) + align_up(m * sizeof(int32_t), 256) +
+         align_up(m * iq::kLatentDim, 256) + iq::kScaleGroups * align_up(m, 4) * sizeof(int32_t);
+}
+
+}  // namespace
+
+extern "C" size_t iq_prepare_q_host_workspace(int M, int fp4_format) {
+  if (M <= 0 || !valid_format(fp4_format)) return 0;
+  return host_ws_bytes(M, iq_fp4_scale_bytes(fp4_format));
+}
+
+extern "C" int iq_set_host_chunk_rows(int rows) {
+  if (rows < kHostChunkAlign) rows = kHostChunkAlign;
+  if (rows > (1 << 20)) rows = 1 << 20;
+  rows = (rows + kHostChunkAlign - 1) / kHostChunkAlign * kHostChunkAlign;
+  return g_host_chunk_rows.exchange(rows);
+}
+
+extern "C" int iq_host_chunk_rows(void) { return g_host_chunk_rows.load(); }
+
+extern "C" iq_status iq_prepare_q_host(const void* latent_bf16, int M, const void* wq_e4m3, const uint8_t* wq_sf,
+                                       const int32_t* positions, int fp4_format, uint8_t* q_fp4, uint8_t* q_sf,
+                                       void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  iq_status st =
+      check_prepare_args(latent_bf16, M, wq_e4m3, wq_sf, positions, q_fp4, q_sf, nullptr, false, fp4_format);
+  if (st != IQ_OK || M == 0) return st;
+  if (!workspace) return IQ_ERR_ARG;
+  if (!aligned(workspace, 256)) return IQ_ERR_ALIGN;
+  const size_t sfb = iq_fp4_scale_bytes(fp4_format);
+  if (ws_bytes < host_ws_bytes(M, sfb)) return IQ_ERR_WORKSPACE;
+  int max_pairs = 0, sm_count = 0;
+  st = device_setup(&max_pairs, &sm_count);
+  if (st != IQ_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IQ_ERR_CUDA;
+  const uint16_t* lat = static_cast<const uint16_t*>(device_view(latent_bf16, dev));
+  const int32_t* pos_src = static_cast<const int32_t*>(device_view(positions, dev));
+  if (!lat || !pos_src || !device_view(q_fp4, dev) || !device_view(q_sf, dev)) return IQ_ERR_ARG;
+
+  HostPath& h = g_host[dev];
+  std::lock_guard<std::mutex> lock(h.mu);
+  st = host_path_setup(h);
+  if (st != IQ_OK) return st;
+
+  const size_t m = static_cast<size_t>(M);
+  uint8_t* q_dev = static_cast<uint8_t*>(workspace);
+  uint8_t* sf_dev = q_dev + align_up(m * (iq::kQDim / 2), 256);
+  int32_t* pos_dev = reinterpret_cast<int32_t*>(sf_dev + align_up(m * sfb, 256));
+  uint8_t* xq = reinterpret_cast<uint8_t*>(pos_dev) + align_up(m * sizeof(int32_t), 256);
+  int32_t* x_sf = reinterpret_cast<int32_t*>(xq + align_up(m * iq::kLatentDim, 256));
+
+  int rows = g_host_chunk_rows.load(std::memory_order_relaxed);
+  const int min_rows = (M + kMaxHostChunks - 1) / kMaxHostChunks;
+  if (rows < min_rows) rows = (min_rows + kHostChunkAlign - 1) / kHostChunkAlign * kHostChunkAlign;
+  const int chunks = (M + rows - 1) / rows;
+
+  bool ok = cudaEventRecord(h.fork, stream) == cudaSuccess && cudaStreamWaitEvent(h.in, h.fork, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(h.comp, h.fork, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(h.out, h.fork, 0) == cudaSuccess;
+  for (int c = 0; ok && c < chunks; ++c) {
+    const int r0 = c * rows;
+    const int mc = M - r0 < rows ? M - r0 : rows;
+    const size_t q_off = static_cast<size_t>(r0) * (iq::kQDim / 2), sf_off = static_cast<size_t>(r0) * sfb;
+    uint8_t* xq_c = xq + static_cast<size_t>(r0) * iq::kLatentDim;
+    int32_t* x_sf_c = x_sf + static_cast<size_t>(iq::kScaleGroups) * r0;
+    ok = iq::launch_quant_1x128_host_rows(lat + static_cast<size_t>(r0) * iq::kLatentDim, mc, iq::kLatentDim,
+                                          iq::kLatentDim, xq_c, iq::kLatentDim, x_sf_c, pos_src + r0, pos_dev + r0,
+                                          sm_count, h.in) == cudaSuccess &&
+         cudaEventRecord(h.in_done[c], h.in) == cudaSuccess &&
+         cudaStreamWaitEvent(h.comp, h.in_done[c], 0) == cudaSuccess;
+    if (ok) {
+      st = gemm_stage(xq_c, x_sf_c, mc, wq_e4m3, wq_sf, pos_dev + r0, q_dev + q_off, sf_dev + sf_off, nullptr,
+                      fp4_format, max_pairs, h.comp);
+      ok = st == IQ_OK;
+    }
+    ok = ok && cudaEventRecord(h.comp_done[c], h.comp) == cudaSuccess &&
+         cudaStreamWaitEvent(h.out, h.comp_done[c], 0) == cudaSuccess &&
+         cudaMemcpyAsync(q_fp4 + q_off, q_dev + q_off, static_cast<size_t>(mc) * (iq::kQDim / 2), cudaMemcpyDefault,
+                         h.out) == cudaSuccess &&
+         cudaMemcpyAsync(q_sf + sf_off, sf_dev + sf_off, static_cast<size_t>(mc) * sfb, cudaMemcpyDefault, h.out) ==
+             cudaSuccess;
+  }
+  // Join all three streams back into `stream`, also after a failed step, so
+  // that later work on `stream` stays ordered after everything enqueued here.
+  const bool joined = cudaEventRecord(h.tail_in, h.in) == cudaSuccess &&
+                      cudaEventRecord(h.tail_comp, h.comp) == cudaSuccess &&
+                      cudaStreamWaitEvent(h.out, h.tail_in, 0) == cudaSuccess &&
+                      cudaStreamWaitEvent(h.out, h.tail_comp, 0) == cudaSuccess &&
+                      cudaEventRecord(h.join, h.out) == cudaSuccess &&
+                      cudaStreamWaitEvent(stream, h.join, 0) == cudaSuccess;
+  if (st != IQ_OK) return st;
+  return ok && joined ? IQ_OK : IQ_ERR_CUDA;
 }

@@ -71,6 +71,13 @@ enum : uint32_t {
 cudaError_t launch_quant_1x128(const void* x, int M, int K, long long ldx, void* y, long long ldy, int32_t* sf,
                                cudaStream_t stream);
 
+// The quantizer with the lane map for rows in page-locked host memory: the
+// same codes and scales; it also copies the M int32 positions pos_src ->
+// pos_dst, and max_blocks > 0 caps its grid (the warps then loop).
+cudaError_t launch_quant_1x128_host_rows(const void* x, int M, int K, long long ldx, void* y, long long ldy,
+                                         int32_t* sf, const int32_t* pos_src, int32_t* pos_dst, int max_blocks,
+                                         cudaStream_t stream);
+
 // Kernel attribute set-up of the fused GEMM on the current device; returns
 // how many of its CTA pairs fit on the device at once.
 cudaError_t gemm_setup_device(int* max_pairs);

@@ -42,6 +42,10 @@ SIGNATURES = {
     "iq_small_m_threshold": (_I, []),
     "iq_fp4_scale_bytes": (_SZ, [_I]),
     "iq_prepare_q_ex": (_I, [_P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
+    "iq_prepare_q_host_workspace": (_SZ, [_I, _I]),
+    "iq_prepare_q_host": (_I, [_P, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P]),
+    "iq_set_host_chunk_rows": (_I, [_I]),
+    "iq_host_chunk_rows": (_I, []),
 }
 
 # FP4 output variants (include/iq.h, iq_fp4_format).
@@ -190,6 +194,64 @@ def prepare_q(latent: torch.Tensor, wq: torch.Tensor, wq_sf: torch.Tensor, posit
     _check(lib().iq_prepare_q(_ptr(latent), M, _ptr(wq), _ptr(wq_sf), _ptr(positions), _ptr(q_fp4), _ptr(q_sf),
                               _ptr(workspace), workspace.numel(), _stream(stream)), "iq_prepare_q")
     return q_fp4, q_sf
+
+
+def _require_host_side(t: torch.Tensor, name: str, dtypes, shape):
+    """A page-locked CPU tensor (or a CUDA tensor) of the given dtype and shape."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be in page-locked host memory (tensor.pin_memory()) or on the GPU")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def prepare_q_host_workspace_bytes(M: int, fp4_format: str = "mx") -> int:
+    return int(lib().iq_prepare_q_host_workspace(M, FP4_FORMATS[fp4_format]))
+
+
+def prepare_q_host(latent: torch.Tensor, wq: torch.Tensor, wq_sf: torch.Tensor, positions: torch.Tensor, *,
+                   q_fp4: torch.Tensor | None = None, q_sf: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None, fp4_format: str = "mx", stream=None):
+    """Indexer-Q preparation on host-resident tokens (iq_prepare_q_host):
+    latent [M, 1536] bf16 and positions [M] int32 in page-locked host memory;
+    returns (q_fp4 uint8 [M, 4096], q_sf uint8 [M, 256] or [M, 512]) in
+    page-locked host memory, complete once `stream` reaches the point after
+    this call.  W and its scales are on the GPU."""
+    M = latent.shape[0]
+    if fp4_format not in FP4_FORMATS:
+        raise ValueError(f"fp4_format must be one of {sorted(FP4_FORMATS)}")
+    _require_host_side(latent, "latent", (torch.bfloat16,), (M, LATENT_DIM))
+    _require_host_side(positions, "positions", (torch.int32,), (M,))
+    _require(wq, "wq", _U8, (Q_DIM, LATENT_DIM))
+    _require(wq_sf, "wq_sf", (torch.uint8,), (N_HEADS, LATENT_DIM // 128))
+    sf_cols = Q_DIM // 16 if fp4_format == "nv" else Q_DIM // 32
+    if q_fp4 is None:
+        q_fp4 = torch.empty((M, Q_DIM // 2), dtype=torch.uint8).pin_memory()
+    if q_sf is None:
+        q_sf = torch.empty((M, sf_cols), dtype=torch.uint8).pin_memory()
+    _require_host_side(q_fp4, "q_fp4", (torch.uint8,), (M, Q_DIM // 2))
+    _require_host_side(q_sf, "q_sf", (torch.uint8,), (M, sf_cols))
+    if workspace is None:
+        workspace = torch.empty(max(prepare_q_host_workspace_bytes(M, fp4_format), 1), dtype=torch.uint8,
+                                device=wq.device)
+    _require(workspace, "workspace", (torch.uint8,))
+    _check(lib().iq_prepare_q_host(_ptr(latent), M, _ptr(wq), _ptr(wq_sf), _ptr(positions),
+                                   FP4_FORMATS[fp4_format], _ptr(q_fp4), _ptr(q_sf), _ptr(workspace),
+                                   workspace.numel(), _stream(stream)), "iq_prepare_q_host")
+    return q_fp4, q_sf
+
+
+def set_host_chunk_rows(rows: int) -> int:
+    """Rows per chunk of prepare_q_host (a multiple of 256); returns the
+    previous value."""
+    return int(lib().iq_set_host_chunk_rows(int(rows)))
+
+
+def host_chunk_rows() -> int:
+    return int(lib().iq_host_chunk_rows())
 
 
 def gemm_rope_hadamard_fp4(xq: torch.Tensor, x_scales: torch.Tensor, wq: torch.Tensor, wq_sf: torch.Tensor,

@@ -269,6 +269,59 @@ iq_status iq_prepare_q_static(const void* latent_bf16, int M,
                               const int32_t* positions,
                               uint8_t* q_fp4, uint8_t* q_sf, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Indexer-Q preparation on host-resident tokens.  The pages have no
+ * counterpart of this call; it serves a caller whose token rows and results
+ * live in host memory (an offload or batch job), and overlaps their transfer
+ * with the computation.  Same operation, arguments and results as
+ * iq_prepare_q_ex, except where the buffers live:
+ *
+ *   latent_bf16 [M, 1536] BF16, positions [M] int32   -- read
+ *   q_fp4 [M, 4096] uint8, q_sf [M, iq_fp4_scale_bytes(fp4_format)] uint8
+ *                                                     -- written
+ *     page-locked host memory (cudaHostAlloc / cudaMallocHost, or
+ *     cudaHostRegister), or device memory of the current device; the same
+ *     row-major layouts and alignments as iq_prepare_q.
+ *   wq_e4m3, wq_sf: device memory, as in iq_prepare_q.
+ *   workspace: iq_prepare_q_host_workspace(M, fp4_format) bytes of device
+ *     memory, 256-byte aligned, used until the call's work completes.
+ *
+ * The rows are processed in chunks of iq_host_chunk_rows() rows (fewer
+ * chunks when M needs more than 64).  On internal streams of the device the
+ * quantizer of chunk c reads the chunk's latent rows and positions directly
+ * from host memory, the GEMM of chunk c runs once that is done, and chunk c's
+ * FP4 codes and scales are copied to q_fp4 / q_sf once its GEMM is done; so
+ * reading chunk c + 1, computing chunk c and returning chunk c - 1 overlap.
+ *
+ * Ordering: the work starts after everything enqueued on `stream` before the
+ * call, and everything enqueued on `stream` after the call starts after all
+ * of it, the copies into q_fp4 / q_sf included.  Synchronize `stream` (or an
+ * event recorded on it after the call) before reading the results on the
+ * host, and leave the inputs unchanged until then.
+ *
+ * Errors: those of iq_prepare_q_ex, and IQ_ERR_ARG when latent_bf16,
+ * positions, q_fp4 or q_sf is pageable host memory or another device's
+ * memory, or the workspace is NULL; IQ_ERR_WORKSPACE when ws_bytes is smaller
+ * than iq_prepare_q_host_workspace(M, fp4_format).  M == 0 returns IQ_OK.
+ *
+ * The first call on a device creates three streams and 132 events there
+ * (kept until the process exits); make it outside stream capture.  Calls on
+ * one device enqueue one at a time (a lock) because they share those streams.
+ * ------------------------------------------------------------------------ */
+
+size_t iq_prepare_q_host_workspace(int M, int fp4_format);
+
+iq_status iq_prepare_q_host(const void* latent_bf16, int M,
+                            const void* wq_e4m3, const uint8_t* wq_sf,
+                            const int32_t* positions, int fp4_format,
+                            uint8_t* q_fp4, uint8_t* q_sf,
+                            void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Rows per chunk of iq_prepare_q_host, rounded up to a multiple of 256 and
+ * clamped to [256, 2^20]; returns the previous value (default 1024). */
+int iq_set_host_chunk_rows(int rows);
+int iq_host_chunk_rows(void);
+
 #ifdef __cplusplus
 }
 #endif

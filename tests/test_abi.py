@@ -106,3 +106,34 @@ def test_fp4_format_helpers_and_checks(lib):
     # NVFP4 scales need 8-byte alignment
     assert lib.iq_prepare_q_ex(16, 4, 16, 16, 16, 2, 16, 20, None, 256, 1 << 20, None) == -2
     assert lib.iq_prepare_q_ex(16, 0, 16, 16, 16, 2, 16, 20, None, None, 0, None) == 0
+
+
+def test_host_entry_sizes_settings_and_checks(lib):
+    """iq_prepare_q_host: workspace size, chunk-row setting, and the argument
+    checks that come before any CUDA call."""
+    # codes + scales + positions + FP8 latent + packed scales, each 256-aligned
+    assert lib.iq_prepare_q_host_workspace(4632, 0) == 4632 * 4096 + 4632 * 256 + 18688 + 4632 * 1536 + 3 * 4632 * 4
+    assert lib.iq_prepare_q_host_workspace(4632, 2) == 4632 * 4096 + 4632 * 512 + 18688 + 4632 * 1536 + 3 * 4632 * 4
+    assert lib.iq_prepare_q_host_workspace(5, 0) == 20480 + 1280 + 256 + 7680 + 3 * 8 * 4
+    assert lib.iq_prepare_q_host_workspace(0, 0) == 0
+    assert lib.iq_prepare_q_host_workspace(16, 9) == 0
+    old = lib.iq_host_chunk_rows()
+    try:
+        assert lib.iq_set_host_chunk_rows(300) == old
+        assert lib.iq_host_chunk_rows() == 512
+        lib.iq_set_host_chunk_rows(1)
+        assert lib.iq_host_chunk_rows() == 256
+        lib.iq_set_host_chunk_rows(1 << 30)
+        assert lib.iq_host_chunk_rows() == 1 << 20
+    finally:
+        lib.iq_set_host_chunk_rows(old)
+    assert lib.iq_host_chunk_rows() == old
+    need = lib.iq_prepare_q_host_workspace(4, 0)
+    assert lib.iq_prepare_q_host(16, 0, 16, 16, 16, 0, 16, 16, None, 0, None) == 0       # M == 0
+    assert lib.iq_prepare_q_host(16, -1, 16, 16, 16, 0, 16, 16, 256, need, None) == -1   # M < 0
+    assert lib.iq_prepare_q_host(16, 4, 16, 16, 16, 5, 16, 16, 256, need, None) == -1    # unknown format
+    assert lib.iq_prepare_q_host(16, 4, 16, 16, 16, 0, 16, 16, None, need, None) == -1   # no workspace
+    assert lib.iq_prepare_q_host(16, 4, 16, 16, 16, 0, 16, 16, 128, need, None) == -2    # workspace alignment
+    assert lib.iq_prepare_q_host(16, 4, 16, 16, 16, 0, 16, 16, 256, need - 1, None) == -6
+    assert lib.iq_prepare_q_host(24, 4, 16, 16, 16, 0, 16, 16, 256, need, None) == -2    # latent alignment
+
