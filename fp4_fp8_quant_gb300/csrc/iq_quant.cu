@@ -42,7 +42,11 @@ namespace iq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kHostThreads = 256;
+// Host-rows variant: 128 threads (4K registers) per block, so that two of its
+// blocks fit on an SM beside a CTA of the GEMM kernel (53.8K registers, 224 KB
+// of shared memory; each further block reserves 1 KB) whatever way the
+// blocks are spread; one block per SM keeps ~0.6 MB of loads in flight.
+constexpr int kHostThreads = 128;
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 r;
