@@ -9,8 +9,9 @@ synthetic data resident in HBM before the timed region; L2 is flushed (256 MB wr
 lines are left for the timed kernels to write back) between timed steps,
 outside the CUDA-event intervals.  Also measured in the same run: the quantizer alone on
 BF16 [4632, 7168] (GB/s against HBM), the GEMM's own launch time (for the
-roofline), the end-to-end call with pinned host buffers (copies inside the
-timed region), decode steps replayed from a CUDA graph (1, 8, 32, 64
+roofline), the end-to-end call iq_prepare_q_host on page-locked host
+buffers (the latent read from and the FP4 output written to host memory
+inside the timed region), decode steps replayed from a CUDA graph (1, 8, 32, 64
 tokens), a token sweep (128 ... 65536), the step with each FP4 output
 variant, and the CPU oracle on a bounded sample of the same workload.
 

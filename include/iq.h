@@ -34,9 +34,11 @@
  * were enqueued; a device-side wait that ran out of time is recorded in the
  * device status word (iq_device_status).
  *
- * Thread safety: calls may be made from several host threads; the only shared
- * host state is the per-device set-up done on the first call on a device
- * (architecture check, kernel attributes), which is guarded.
+ * Thread safety: calls may be made from several host threads.  Shared host
+ * state: the per-device set-up done on the first call on a device
+ * (architecture check, kernel attributes), which is guarded, and the
+ * internal streams and events of iq_prepare_q_host, whose calls on one device
+ * enqueue one at a time under a lock.
  */
 #ifndef IQ_H_
 #define IQ_H_
