@@ -490,6 +490,10 @@ extern "C" iq_status iq_prepare_q_host(const void* latent_bf16, int M, const voi
          cudaEventRecord(h.in_done[c], h.in) == cudaSuccess &&
          cudaStreamWaitEvent(h.comp, h.in_done[c], 0) == cudaSuccess;
     if (ok) {
+      // The GEMM kernels are launched with programmatic stream serialization
+      // but never trigger an early launch themselves, so a chunk's GEMM starts
+      // after the previous chunk's has completed, and after the event wait
+      // above (its inputs come from another stream).
       st = gemm_stage(xq_c, x_sf_c, mc, wq_e4m3, wq_sf, pos_dev + r0, q_dev + q_off, sf_dev + sf_off, nullptr,
                       fp4_format, max_pairs, h.comp);
       ok = st == IQ_OK;
