@@ -7,7 +7,9 @@ fused block-scaled FP8 GEMM with the RoPE -> Hadamard -> FP4 epilogue
 [4632, 4096] and its UE8M0 scales [4632, 256].  Inputs are seeded
 synthetic data resident in HBM before the timed region; L2 is flushed (256 MB written, then 256 MB read, so no dirty
 lines are left for the timed kernels to write back) between timed steps,
-outside the CUDA-event intervals.  Also measured in the same run: the quantizer alone on
+outside the CUDA-event intervals.  `value` is the token count over the median
+of the K event-timed steps (mean, minimum and maximum are reported beside it);
+the warm-up runs at least W steps and at least half a second.  Also measured in the same run: the quantizer alone on
 BF16 [4632, 7168] (GB/s against HBM), the GEMM's own launch time (for the
 roofline), the end-to-end call iq_prepare_q_host on page-locked host
 buffers (the latent read from and the FP4 output written to host memory
@@ -46,6 +48,9 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0            # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 ORACLE_SAMPLE_ROWS = 4632      # rows of the prefill workload per oracle timing (all of it)
+WARMUP_MIN_S = 0.5             # the warm-up also lasts at least this long (clocks leave idle)
+NOMINAL_HBM_GBS = 7900.0       # HBM3e nominal bandwidth of GB300
+NOMINAL_FP8_TFLOPS = 4500.0    # dense FP8 tensor nominal of GB300
 
 
 def parse():
@@ -123,8 +128,8 @@ def kernel_traffic(kernel_key: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks sampled every 20 ms from the start of the chain's timed
-    region to the end of the end-to-end measurement."""
+    """nvidia-smi clocks sampled every 20 ms from the start of the chain's
+    warm-up to the end of the end-to-end measurement."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -182,6 +187,51 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def cublas_fp8_tflops(dev, n: int = 8192, reps: int = 20):
+    """Dense FP8 (E4M3 x E4M3 -> BF16, per-tensor scales) throughput of the
+    vendor library on an n^3 GEMM, best of `reps` launches: a measured FP8
+    tensor-core rate on this GPU to set beside the BF16-derived peak.  None
+    when the library call is not available."""
+    import torch
+    try:
+        a = torch.randn((n, n), device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device=dev).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=dev, dtype=torch.float32)
+        for _ in range(3):
+            torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except (RuntimeError, AttributeError, TypeError):
+        return None
+
+
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def oracle_sample_seconds(rows: int) -> float:
     """Times the CPU oracle (single thread) on the first `rows` tokens of the
     prefill workload in a child process, so the BLAS thread count is pinned."""
@@ -228,7 +278,7 @@ def run_reference(args):
                                "positions 0..4631 (oracle: a 256-token slice per step)", "M": M_PREFILL},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": "a 256-token slice of the 4632-token prefill workload per step, FP64 numpy, "
-                                   "one thread"},
+                                   "one thread", "cpu_model": host_cpu_model(), "host_cores": os.cpu_count()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -283,11 +333,21 @@ def run_ours(args):
         # dependent (no host or event work between the two launches).
         iq.prepare_q(lat, w, ws, p, q_fp4=q, q_sf=s, workspace=work)
 
-    for _ in range(max(3, args.warmup)):
+    # The clock sampler starts before the warm-up, so its start-up and the
+    # clocks' ramp from idle both fall before the timed steps.  The warm-up is
+    # at least W steps (each after an L2 flush, as timed) and at least
+    # WARMUP_MIN_S of them.
+    clocks = ClockSampler(local).__enter__()
+    t0 = time.perf_counter()
+    n_warm = 0
+    while n_warm < max(3, args.warmup) or time.perf_counter() - t0 < WARMUP_MIN_S:
+        flush_l2()
         step()
+        n_warm += 1
+        if n_warm % 16 == 0:
+            torch.cuda.synchronize()
     barrier()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    clocks = ClockSampler(local).__enter__()
     barrier()
     t_wall = time.perf_counter()
     for i in range(args.steps):
@@ -298,8 +358,10 @@ def run_ours(args):
     barrier()
     t_wall = time.perf_counter() - t_wall
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    ms_per_step = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
+    ms_per_step = max_over_ranks(statistics.median(step_ms), world, dev)
     value = whole_job_rate(M, world, ms_per_step)
+    step_stats = {"median_ms": statistics.median(step_ms), "mean_ms": sum(step_ms) / len(step_ms),
+                  "min_ms": min(step_ms), "max_ms": max(step_ms), "warmup_steps_run": n_warm}
 
     # The fused GEMM's own launch duration (for the roofline): the same
     # launches with events around the GEMM alone (the quantizer runs first,
@@ -312,7 +374,8 @@ def run_ours(args):
         iq.gemm_rope_hadamard_fp4(xq, xs, w, ws, p, q_fp4=q, q_sf=s)
         b.record(stream)
     torch.cuda.synchronize()
-    k2_avg_ms = sum(a.elapsed_time(b) for a, b in k2ev) / len(k2ev)
+    k2_ms = [a.elapsed_time(b) for a, b in k2ev]
+    k2_avg_ms = sum(k2_ms) / len(k2_ms)
     k1ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a, b in k1ev:
         flush_l2()
@@ -325,11 +388,16 @@ def run_ours(args):
     hbm_peak, bf16_peak, peak_kind = load_peaks()
     fp8_peak_tflops = bf16_peak * FP8_OVER_BF16
     achieved_tflops = M * FLOPS_PER_TOKEN / (k2_avg_ms * 1e-3) / 1e12
+    cublas_fp8 = cublas_fp8_tflops(dev)
     roofline = {"kernel": "gemm_rope_hadamard_fp4_kernel", "bound": "tensor", "achieved": achieved_tflops,
                 "peak": fp8_peak_tflops, "unit": "TFLOP/s", "frac": achieved_tflops / fp8_peak_tflops,
                 "traffic": kernel_traffic("gemm_rope_hadamard_fp4_kernel"),
                 "peak_source": f"{peak_kind} bf16 x {FP8_OVER_BF16:g} (FP8/BF16 nominal ratio)",
-                "avg_launch_ms": k2_avg_ms, "flops_per_launch": M * FLOPS_PER_TOKEN}
+                "avg_launch_ms": k2_avg_ms, "median_launch_ms": statistics.median(k2_ms),
+                "flops_per_launch": M * FLOPS_PER_TOKEN,
+                "frac_of_nominal_fp8": achieved_tflops / NOMINAL_FP8_TFLOPS,
+                "cublas_fp8_tflops_same_run": cublas_fp8,
+                "frac_of_cublas_fp8": achieved_tflops / cublas_fp8 if cublas_fp8 else None}
 
     # ------------------------------------- FP4 output variants (prefill step)
     # The same step with each FP4 output variant of iq_prepare_q_ex (L2
@@ -373,7 +441,8 @@ def run_ours(args):
                  "avg_launch_ms": q_ms,
                  "roofline": {"kernel": "quant_1x128_kernel", "bound": "hbm", "achieved": q_gbs, "peak": hbm_peak,
                               "unit": "GB/s", "frac": q_gbs / hbm_peak, "traffic": kernel_traffic("quant_1x128_kernel"),
-                              "peak_source": peak_kind, "bytes_per_launch": q_bytes}}
+                              "peak_source": peak_kind, "bytes_per_launch": q_bytes,
+                              "frac_of_nominal_hbm": q_gbs / NOMINAL_HBM_GBS}}
 
     # ------------------------------------------- decode under graph replay
     # Decode steps (N(0,1) latent, random positions) captured in a CUDA graph
@@ -494,6 +563,11 @@ def run_ours(args):
             "chain_tflops": flops / (c_ms * 1e-3) / 1e12, "chain_frac_of_fp8_peak": flops / (c_ms * 1e-3) / 1e12 / fp8_peak_tflops,
             "quant7168_us": qs_ms * 1e3, "quant7168_gbs": qbytes / (qs_ms * 1e-3) / 1e9,
             "quant7168_frac_of_hbm": qbytes / (qs_ms * 1e-3) / 1e9 / hbm_peak}
+    # The quantizer's fraction also against the best rate any of its launches
+    # reached in this run (the copy-measured peak is not a ceiling for it).
+    best_q = max([q_gbs] + [v["quant7168_gbs"] for v in sweep.values()])
+    quantizer["roofline"]["best_kernel_gbs_in_run"] = best_q
+    quantizer["roofline"]["frac_of_best_in_run"] = q_gbs / best_q
 
     # ------------------------------------------ end to end through the C ABI
     # iq_prepare_q_host on page-locked host buffers: every step reads the
@@ -530,7 +604,8 @@ def run_ours(args):
         secs = oracle_sample_seconds(ORACLE_SAMPLE_ROWS)
         cpu = {"value": ORACLE_SAMPLE_ROWS / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"all {ORACLE_SAMPLE_ROWS} tokens of the prefill workload, FP64 numpy, "
-                         f"one thread ({secs:.1f} s)"}
+                         f"one thread ({secs:.1f} s)",
+               "cpu_model": host_cpu_model(), "host_cores": os.cpu_count()}
 
     if rank == 0:
         line = {
@@ -546,7 +621,7 @@ def run_ours(args):
             "roofline": roofline, "quantizer": quantizer, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": 2 * args.steps,
             "clocks": clocks.summary(),
-            "k1_chain_avg_ms": k1_avg_ms, "wall_s_timed": t_wall,
+            "k1_chain_avg_ms": k1_avg_ms, "wall_s_timed": t_wall, "step_stats": step_stats,
             "decode": decode, "sweep": sweep, "fp4_formats": fp4_formats,
         }
         print(json.dumps(line), flush=True)

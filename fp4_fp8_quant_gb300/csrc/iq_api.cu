@@ -1,6 +1,7 @@
 // C-ABI entry points of the indexer-Q preparation library (include/iq.h):
 // argument checks, per-device set-up, TMA descriptor encoding and launches.
-// Nothing here allocates device memory or synchronizes a stream.
+// Nothing here allocates device memory; only the diagnostics
+// (iq_device_status, iq_selftest_wait_timeout) synchronize.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -29,6 +30,7 @@ struct DeviceInfo {
 
 std::mutex g_setup_mutex;
 DeviceInfo g_devices[kMaxDevices];
+std::atomic<int> g_fail_setups{0};   // test hook: set-ups to fail on purpose
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_small_m_max{iq::kSmallMMax};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
@@ -36,39 +38,50 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // First call on a device: check the architecture, set kernel attributes and
-// resolve the driver's tensor-map encoder.  Later calls only read the cache.
+// resolve the driver's tensor-map encoder.  Success and a wrong architecture
+// are cached (later calls only read the cache); a failed CUDA call is not, so
+// the next call tries again (a transient failure, e.g. a first call made
+// while the stream is being captured, does not disable the device for good).
 iq_status device_setup(int* max_pairs, int* sm_count = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return IQ_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   DeviceInfo& d = g_devices[dev];
   if (!d.ready) {
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
-      return IQ_ERR_CUDA;
-    }
-    if (major != 10 || minor != 3) {
-      d.status = IQ_ERR_ARCH;
-    } else if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-      d.status = IQ_ERR_CUDA;
-    } else if (iq::gemm_setup_device(&d.max_pairs) != cudaSuccess || d.max_pairs < 1 ||
+    int major = 0, minor = 0, sms = 0, pairs = 0;
+    iq_status status = IQ_OK;
+    if (g_fail_setups.load() > 0) {
+      g_fail_setups.fetch_sub(1);
+      status = IQ_ERR_CUDA;
+    } else if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+               cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      status = IQ_ERR_CUDA;
+    } else if (major != 10 || minor != 3) {
+      status = IQ_ERR_ARCH;
+    } else if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      status = IQ_ERR_CUDA;
+    } else if (iq::gemm_setup_device(&pairs) != cudaSuccess || pairs < 1 ||
                iq::small_m_setup_device() != cudaSuccess) {
-      d.status = IQ_ERR_CUDA;
-    } else {
-      d.status = IQ_OK;
+      status = IQ_ERR_CUDA;
     }
-    if (d.status == IQ_OK && g_encode_tiled == nullptr) {
+    if (status == IQ_OK && g_encode_tiled == nullptr) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
       if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
               cudaSuccess ||
           q != cudaDriverEntryPointSuccess || fn == nullptr) {
-        d.status = IQ_ERR_CUDA;
+        status = IQ_ERR_CUDA;
       } else {
         g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
       }
     }
+    if (status == IQ_ERR_CUDA) {
+      (void)cudaGetLastError();   // reset the runtime's last-error state for the retry
+      return status;
+    }
+    d.sm_count = sms;
+    d.max_pairs = pairs;
+    d.status = status;
     d.ready = true;
   }
   *max_pairs = d.max_pairs;
@@ -203,6 +216,67 @@ iq_status iq_device_status(uint32_t* flags, int reset) {
 }
 
 void iq_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs); }
+
+void iq_debug_fail_next_setups(int count) { g_fail_setups.store(count > 0 ? count : 0); }
+
+size_t iq_selftest_workspace(void) {
+  // x_sf [3][256] words, positions [256], w_sf [64][12] bytes, q_sf [256][256]
+  // bytes, q_fp4 [256][4096] bytes, each at a 256-byte boundary.
+  return align_up(3 * 256 * 4, 256) + align_up(256 * 4, 256) + align_up(64 * 12, 256) + 256 * 256 +
+         static_cast<size_t>(256) * 4096;
+}
+
+iq_status iq_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t timeout_ns, uint32_t* flags,
+                                   cudaStream_t stream) {
+  if (!workspace || timeout_ns == 0) return IQ_ERR_ARG;
+  if (!aligned(workspace, 256)) return IQ_ERR_ALIGN;
+  if (ws_bytes < iq_selftest_workspace()) return IQ_ERR_WORKSPACE;
+  int max_pairs = 0;
+  iq_status st = device_setup(&max_pairs);
+  if (st != IQ_OK) return st;
+  // Start from a clean status word, so the bits read afterwards are this
+  // launch's alone.
+  if (cudaStreamSynchronize(stream) != cudaSuccess || iq_device_status(nullptr, 1) == IQ_ERR_CUDA) return IQ_ERR_CUDA;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  int32_t* x_sf = reinterpret_cast<int32_t*>(base);
+  int32_t* pos = reinterpret_cast<int32_t*>(base + align_up(3 * 256 * 4, 256));
+  uint8_t* w_sf = reinterpret_cast<uint8_t*>(pos) + align_up(256 * 4, 256);
+  uint8_t* q_sf = w_sf + align_up(64 * 12, 256);
+  uint8_t* q_fp4 = q_sf + 256 * 256;
+  if (cudaMemsetAsync(workspace, 0, iq_selftest_workspace(), stream) != cudaSuccess) return IQ_ERR_CUDA;
+  const int M = 256;
+  static const iq::RopeTurns rope = make_rope_turns();
+  iq::GemmArgs a;
+  a.x_sf = x_sf;
+  a.w_sf = w_sf;
+  a.pos = pos;
+  a.q_fp4 = q_fp4;
+  a.q_sf = q_sf;
+  a.q_pre = nullptr;
+  a.M = M;
+  a.m_al = M;
+  a.num_m_tiles = M / 128;
+  a.num_m_pairs = 1;
+  a.num_pair_tiles = iq::kQDim / 256;
+  a.timeout_ns = timeout_ns;
+  a.rope = rope;
+  // The tensor maps are valid descriptors over the workspace (nothing is
+  // loaded through them; the store map is never used either).
+  CUtensorMap tm_x, tm_w, tm_q;
+  if (!encode_2d_u8(&tm_x, q_fp4, iq::kLatentDim, 256, 128, 128) ||
+      !encode_2d_u8(&tm_w, q_fp4, iq::kLatentDim, 256, 128, 128) ||
+      !encode_2d_u8(&tm_q, q_fp4, iq::kQDim / 2, 256, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) {
+    return IQ_ERR_CUDA;
+  }
+  if (iq::launch_gemm_wait_selftest(tm_x, tm_w, tm_q, a, max_pairs, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess) {
+    return IQ_ERR_CUDA;
+  }
+  uint32_t v = 0;
+  st = iq_device_status(&v, 1);
+  if (flags) *flags = v;
+  return st;
+}
 
 int iq_set_small_m_threshold(int max_tokens) {
   const int v = max_tokens < 0 ? 0 : (max_tokens > iq::kSmallMMax ? iq::kSmallMMax : max_tokens);

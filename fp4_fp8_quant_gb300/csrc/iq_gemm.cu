@@ -249,7 +249,13 @@ __device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int hea
   }
 }
 
-template <int kFmt>
+// kNoLoads: the wait self-test instance.  Its producer issues no TMA loads,
+// so the stage barriers the MMA issuer waits on never complete, no MMA is
+// issued, and the MMA issuer's, the epilogue's and the producer's bounded
+// waits all give up with nothing asynchronous in flight (the only tensor-core
+// work is the scale-factor copy, which completes).  It exercises the give-up
+// and teardown path; the product launches only kNoLoads = false.
+template <int kFmt, bool kNoLoads = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_rope_hadamard_fp4_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ GemmArgs args) {
@@ -401,13 +407,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(&full[stage], kPairStageTx);
-          const uint32_t bar = full_leader0 + 8u * stage;
-          tma_load_2d_pair(sA + stage * kABytes, &tm_x, bar, kb * BK, m0);
-          tma_load_2d_pair(sB + stage * kBBytes, &tm_w, bar, kb * BK,
-                           n_tile * BN + static_cast<int>(rank) * (BN / kPair));
-          issued_mask |= 1u << stage;
-          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if constexpr (!kNoLoads) {
+            if (leader) mbar_arrive_expect_tx(&full[stage], kPairStageTx);
+            const uint32_t bar = full_leader0 + 8u * stage;
+            tma_load_2d_pair(sA + stage * kABytes, &tm_x, bar, kb * BK, m0);
+            tma_load_2d_pair(sB + stage * kBBytes, &tm_w, bar, kb * BK,
+                             n_tile * BN + static_cast<int>(rank) * (BN / kPair));
+            issued_mask |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          }
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -608,6 +616,17 @@ cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtenso
     case kFp4Nv: return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel<kFp4Nv>, tm_x, tm_w, tm_q, args);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_gemm_wait_selftest(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
+                                      const GemmArgs& args, int max_pairs, cudaStream_t stream) {
+  const cudaError_t err = cudaFuncSetAttribute(gemm_rope_hadamard_fp4_kernel<kFp4Mx, true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const int pairs = args.num_pair_tiles < max_pairs ? args.num_pair_tiles : max_pairs;
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pair_config(pairs, attr, stream);
+  return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel<kFp4Mx, true>, tm_x, tm_w, tm_q, args);
 }
 
 cudaError_t read_device_status(uint32_t* flags, bool reset) {

@@ -87,6 +87,11 @@ int gemm_pair_size();
 cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
                                           const GemmArgs& args, int fp4_format, int max_pairs, cudaStream_t stream);
 
+// The fused GEMM kernel's wait self-test instance (no TMA loads: every wait
+// that depends on them gives up after args.timeout_ns).
+cudaError_t launch_gemm_wait_selftest(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
+                                      const GemmArgs& args, int max_pairs, cudaStream_t stream);
+
 // The small-M (swapped-operand) kernel: M <= kSmallMMax tokens, one launch
 // of 64 clusters of two CTAs (one per K half).
 cudaError_t small_m_setup_device();

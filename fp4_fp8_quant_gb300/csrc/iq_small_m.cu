@@ -50,8 +50,10 @@
 //
 // Every mbarrier wait is bounded (GemmArgs::timeout_ns); a wait that gives up
 // records its kind in this kernel's device status word.  No thread leaves a
-// loop or the kernel early, so every thread of both CTAs reaches the one
-// cluster barrier (arrive after set-up, wait before the exchange) exactly once.
+// loop or the kernel early, so every thread of both CTAs reaches both uses of
+// the cluster barrier exactly once: arrive after set-up, wait before the
+// exchange (the peer is running); arrive after the exchange, wait at the end
+// (the peer has issued its stores into this CTA, even when a wait gave up).
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -333,7 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_async_cluster_f32(red_to[j & 1] + static_cast<uint32_t>((t >> 1) * kHeadDim * 4), v[j], bar_to[j & 1]);
     }
   }
-  if (!mbar_wait(red_full, 0, timeout)) fail(abort_flag, kStatusEpilogueWait);
+  const bool red_ok = mbar_wait(red_full, 0, timeout);
+  if (!red_ok) fail(abort_flag, kStatusEpilogueWait);
+  // Second use of the cluster barrier: this CTA has issued every store into
+  // the peer.  Its wait, at the very end, keeps each CTA resident until the
+  // peer has issued all of its stores into it (see the end of the kernel).
+  cluster_arrive_relaxed();
   // Every thread has read its tensor memory: release it.
   __syncthreads();
   if (warp == 1) {
@@ -447,6 +454,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // stores into this CTA's shared memory completed before red_full did; this
   // CTA's stores into the peer completed before the peer passed its red_full
   // wait, so neither CTA touches the other's shared memory after the exchange.
+  // If a red_full wait gave up, the peer may be late: the cluster wait below
+  // returns once the peer has issued all its stores into this CTA (its arrive
+  // follows them), and a bounded second wait on red_full lets them land before
+  // this CTA's shared memory is released.
+  cluster_wait();
+  if (!red_ok && threadIdx.x == 0) {
+    if (!mbar_wait(red_full, 0, timeout)) fail(abort_flag, kStatusTeardownWait);
+  }
+  __syncthreads();
 }
 
 cudaLaunchConfig_t small_m_config(cudaLaunchAttribute* attr, cudaStream_t stream) {

@@ -93,6 +93,36 @@ def weights(seed: int = 0, N: int = Q_DIM, K: int = LATENT_DIM):
     return codes, sf
 
 
+SWEEP_ROW_BLOCK = 256        # rows per independently seeded block of the large inputs
+
+
+def sweep_quant_block(M: int, K: int, block: int, seed: int = 4,
+                      outlier_p: float = 0.005, outlier_scale: float = 100.0) -> np.ndarray:
+    """BF16 bits of rows [256 * block, min(M, 256 * (block + 1))) of the
+    stand-alone quantizer input of the long-prefill sweep ([M, K], N(0,1) with
+    0.5% of elements x100).  Each 256-row block has its own seeded stream, so a
+    sample of rows can be regenerated without the whole matrix (which reaches
+    65536 x 7168 elements)."""
+    r0 = block * SWEEP_ROW_BLOCK
+    rows = min(M, r0 + SWEEP_ROW_BLOCK) - r0
+    rng = np.random.Generator(np.random.PCG64([seed, block, K]))
+    x = rng.standard_normal((rows, K), dtype=np.float32)
+    hit = rng.random((rows, K), dtype=np.float32) < np.float32(outlier_p)
+    x = np.where(hit, x * np.float32(outlier_scale), x)
+    return f32_to_bf16_bits(x)
+
+
+def sweep_quant_rows(M: int, K: int, rows, seed: int = 4) -> np.ndarray:
+    """The given rows of the same input (BF16 bits [len(rows), K])."""
+    rows = np.asarray(rows)
+    out = np.empty((len(rows), K), np.uint16)
+    for b in np.unique(rows // SWEEP_ROW_BLOCK):
+        blk = sweep_quant_block(M, K, int(b), seed)
+        sel = rows // SWEEP_ROW_BLOCK == b
+        out[sel] = blk[rows[sel] - int(b) * SWEEP_ROW_BLOCK]
+    return out
+
+
 def positions(M: int, seed: int = 0, contiguous: bool = False) -> np.ndarray:
     """int32 [M] token positions: 0..M-1, or uniform in [0, MAX_POSITION)."""
     if contiguous:

@@ -27,8 +27,9 @@
  *   Element code = round-to-nearest-even(x * 2^-e) in the element format.
  *
  * Memory: the caller owns every buffer (inputs, outputs, workspace).  No call
- * allocates device memory, synchronizes the device or the stream, or falls
- * back to another implementation.  Pointers are device pointers unless stated.
+ * allocates device memory or falls back to another implementation, and none
+ * synchronizes the device or the stream except the diagnostics
+ * (iq_device_status, iq_selftest_wait_timeout).  Pointers are device pointers unless stated.
  * All calls are asynchronous on `stream`; errors detected on the host are
  * returned before anything is launched.  A return of IQ_OK means the launches
  * were enqueued; a device-side wait that ran out of time is recorded in the
@@ -77,6 +78,30 @@ iq_status iq_device_status(uint32_t* flags, int reset);
  * (default 2e9).  0 restores the default.  Applies to later launches from any
  * thread. */
 void iq_set_wait_timeout_ns(uint64_t ns);
+
+/* Diagnostics of the failure handling (no counterpart on the pages).
+ *
+ * iq_selftest_wait_timeout runs the fused GEMM kernel once on a 256-token
+ * problem with its TMA loads left out: the stage barriers its MMA issuer
+ * waits on never complete, no MMA is issued, and the producer's, the MMA
+ * issuer's and the epilogue's bounded waits give up after timeout_ns with
+ * nothing asynchronous in flight.  The kernel then takes its normal give-up
+ * and teardown path.  The call resets the status word, launches on `stream`,
+ * synchronizes the stream, stores the status bits the launch set in *flags
+ * (may be NULL) and resets the word again.  Returns IQ_ERR_TIMEOUT when some
+ * wait gave up (the expected result: bits 0, 1 and 2 -- producer, MMA issuer,
+ * epilogue -- set, bit 3 -- teardown -- clear), IQ_OK when none did.
+ * workspace: iq_selftest_workspace() bytes of device memory, 256-byte
+ * aligned, overwritten.  Errors: IQ_ERR_ARG (NULL workspace, timeout 0),
+ * IQ_ERR_ALIGN, IQ_ERR_WORKSPACE, IQ_ERR_CUDA, IQ_ERR_ARCH. */
+size_t iq_selftest_workspace(void);
+iq_status iq_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t timeout_ns, uint32_t* flags,
+                                   cudaStream_t stream);
+
+/* Test hook: the next `count` per-device set-ups (the work of the first call
+ * on a device) fail as if a CUDA query had failed and return IQ_ERR_CUDA.  A
+ * failed set-up is not cached: the next call on the device tries again. */
+void iq_debug_fail_next_setups(int count);
 
 /* Token-count route of the fused GEMM (operation 2).  Calls with
  * 1 <= M <= threshold run the small-M kernel, which swaps the MMA operands

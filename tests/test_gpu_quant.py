@@ -97,3 +97,49 @@ def test_quantizer_empty_and_errors(cuda_device):
     assert L.iq_fp8_quant_1x128_ue8m0(None, 8, 128, 256, y.data_ptr(), 256, s.data_ptr(), st) == -1
     assert L.iq_fp8_quant_1x128_ue8m0(x.data_ptr(), -1, 128, 256, y.data_ptr(), 256, s.data_ptr(), st) == -1
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("M", [16384, 65536])
+def test_quantizer_long_prefill_sweep_sizes(cuda_device, M):
+    """The sweep's quantizer leg, BF16 [M, 7168] with 0.5% of elements x100
+    (up to 114,688 warps and 470 M elements per launch).  Rows are
+    independent: a seeded sample of rows (the first and last, and rows around
+    the 4-row scale-word groups) is compared with the oracle bit for bit; every
+    row is checked on the device against the scale rule and the E4M3 rounding
+    bound."""
+    K = 7168
+    iq = _iq()
+    x = torch.empty((M, K), dtype=torch.int16, device="cuda")
+    for b in range((M + W.SWEEP_ROW_BLOCK - 1) // W.SWEEP_ROW_BLOCK):
+        blk = W.sweep_quant_block(M, K, b)
+        r0 = b * W.SWEEP_ROW_BLOCK
+        x[r0:r0 + blk.shape[0]] = torch.from_numpy(blk.view(np.int16)).cuda()
+    xb = x.view(torch.bfloat16)
+    y, s = iq.fp8_quant_1x128_ue8m0(xb)
+    torch.cuda.synchronize()
+
+    rng = np.random.default_rng(M + 17)
+    rows = np.unique(np.concatenate([rng.choice(M, 60, replace=False), [0, 1, 2, 3, 4, M - 5, M - 1]]))
+    bits = W.sweep_quant_rows(M, K, rows)
+    assert np.array_equal(bits, x[torch.from_numpy(rows).cuda()].cpu().numpy().view(np.uint16))
+    oc, osb = O.quantize_fp8_1x128(O.bf16_bits_to_f64(bits))
+    yc = y[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert np.array_equal(yc, oc), f"{int((yc != oc).sum())} FP8 code mismatches on sampled rows"
+    words = s.cpu().numpy().view(np.uint32)
+    assert words.shape == (K // 512, M)
+    gsb = (words[:, rows].T[:, :, None] >> np.array([0, 8, 16, 24], np.uint32)) & 0xFF
+    assert np.array_equal(gsb.reshape(len(rows), -1)[:, :K // 128], osb)
+
+    # every row: the scale byte is the ceil rule on the floored amax, and each
+    # decoded code lies within half an E4M3 step of x * 2^-e
+    xf = xb.float().view(M, K // 128, 128)
+    e = (words[:, None, :] >> np.array([0, 8, 16, 24], np.uint32)[None, :, None]) & 0xFF
+    e = torch.from_numpy(e.reshape(-1, M).T[:, :K // 128].astype(np.int32) - 127).cuda()
+    amax = xf.abs().amax(dim=2).clamp_min(1e-4)
+    two_e = torch.ldexp(torch.ones_like(amax), e)
+    assert bool(((448.0 * two_e >= amax) & (224.0 * two_e < amax)).all()), "scale exponent breaks the ceil rule"
+    u = xf / two_e[..., None]
+    dec = y.view(torch.float8_e4m3fn).float().view(M, K // 128, 128)
+    _, ex = torch.frexp(u.abs())
+    half_step = torch.ldexp(torch.ones_like(u), torch.clamp(ex - 1, min=-6) - 4)
+    assert bool(((dec - u).abs() <= half_step).all()), "a code lies more than half a step from x * 2^-e"

@@ -413,6 +413,50 @@ def test_one_hot_chain_closed_form():
     check_one_hot_chain()
 
 
+def _rotation_matrix(p):
+    """The 128x128 matrix of the NeoX rotation at position p, built entry by
+    entry: for i < 32 the plane of dims (i, i + 32) turns by p * 10000^(-i/32);
+    dims 64..127 are fixed."""
+    R = np.eye(128)
+    for i in range(32):
+        a = p * 10000.0 ** (-i / 32.0)
+        c, s = math.cos(a), math.sin(a)
+        R[i, i], R[i, i + 32] = c, -s
+        R[i + 32, i], R[i + 32, i + 32] = s, c
+    return R
+
+
+def check_one_hot_chain_at_positions(seed=0):
+    """One-hot latent rows at nonzero positions: Y[n] = W[n, k] again, and each
+    head of the pre-quant Q must be z = H R(p) w / sqrt(128) -- the rotation
+    first, then the transform.  The two do not commute, so a chain that
+    applied the Hadamard transform before RoPE would give H-then-R instead."""
+    import scipy.linalg
+    wq, wsf = W.weights(seed)
+    cols = [5, 300, 1535]
+    pos = np.array([1, 4631, 163839], np.int32)
+    x = np.zeros((3, 1536), np.uint16)
+    for r, k in enumerate(cols):
+        x[r, k] = 0x3F80                    # BF16 1.0
+    _, _, z = O.prepare_q(x, wq, wsf, pos)
+    Hs = scipy.linalg.hadamard(128) / np.sqrt(128)
+    e4 = O.e4m3_value_table()
+    for r, (k, p) in enumerate(zip(cols, pos)):
+        wcol = e4[wq[:, k]] * np.ldexp(1.0, wsf[:, k // 128].astype(np.int64) - 127).repeat(128)
+        R = _rotation_matrix(float(p))
+        want = (Hs @ R @ wcol.reshape(64, 128).T).T.reshape(-1)
+        swapped = (R @ Hs @ wcol.reshape(64, 128).T).T.reshape(-1)
+        assert np.abs(want - swapped).max() > 1e-3 * np.abs(want).max()   # the orders differ here
+        # the angle p * f carries a few float64 ulps of p * f (two routes to
+        # f = 10000^(-i/32) may differ by an ulp): allow that, nothing more
+        tol = (1e-13 + 8.0 * float(p) * 2.0 ** -53) * np.abs(want).max()
+        assert np.allclose(z[r], want, rtol=0, atol=tol), (k, p)
+
+
+def test_one_hot_chain_closed_form_at_nonzero_positions():
+    check_one_hot_chain_at_positions()
+
+
 # ------------------------------------------------- planted mistakes are caught
 
 def _expect_fail(check, monkeypatch, name, bad):
@@ -492,6 +536,23 @@ def test_pins_catch_hadamard_order_error(monkeypatch):
     def bad(n=128):   # a row permutation of a Hadamard matrix is still orthogonal
         return good(n)[::-1].copy()
     _expect_fail(check_hadamard, monkeypatch, "hadamard_matrix", bad)
+
+
+def test_pins_catch_hadamard_before_rope(monkeypatch):
+    """A chain that transforms first and rotates second: rope_neox is made to
+    apply the Hadamard transform and remember the positions, hadamard_heads
+    to apply RoPE with them."""
+    good_rope, good_had = O.rope_neox, O.hadamard_heads
+    seen = {}
+
+    def bad_rope(Y, pos):
+        seen["pos"] = pos
+        return good_had(Y)
+
+    def bad_had(R):
+        return good_rope(R, seen["pos"])
+    monkeypatch.setattr(O, "hadamard_heads", bad_had)
+    _expect_fail(check_one_hot_chain_at_positions, monkeypatch, "rope_neox", bad_rope)
 
 
 def test_pins_catch_rounding_ties_away(monkeypatch):
