@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s) {
         if ((issued_mask >> s) & 1u) {
-          if (!mbar_wait(&empty[s], (issued_phase >> s) & 1u, timeout)) fail(abort_flag, kStatusTeardownWait);
+          if (!mbar_wait(&empty[s], (issued_phase >> s) & 1u, 2 * timeout)) fail(abort_flag, kStatusTeardownWait);
         }
       }
     }
@@ -498,8 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit_pair(final_bar, kPairMask);
       }
       // Teardown (both CTAs): every pair MMA writing this CTA's tensor memory
-      // or reading its shared memory has completed.
-      if (!mbar_wait(final_bar, 0, timeout)) fail(abort_flag, kStatusTeardownWait);
+      // or reading its shared memory has completed.  The teardown waits get
+      // twice the limit: the other CTA's issuer reaches its final commit only
+      // after its own waits, each of which may use the whole limit before it
+      // gives up.
+      if (!mbar_wait(final_bar, 0, 2 * timeout)) fail(abort_flag, kStatusTeardownWait);
     }
     __syncwarp();
   } else {

@@ -196,7 +196,7 @@ def test_fp4_scale_flips_over_the_configs(cuda_device):
     cases += [W.sweep_chain(m) for m in (128, 512, 1024)]
     flips = blocks = zero_flips = codes = 0
     for x, wq, wsf, pos in cases:
-        q, sf, z = _run(x, wq, wsf, pos, debug=False)
+        q, sf = _run(x, wq, wsf, pos, debug=False)
         oq, osf, oz = O.prepare_q(x, wq, wsf, pos)
         st = check_fp4(q, sf, oq, osf, oz)
         flips += st["scale_mismatch_blocks"]
