@@ -33,6 +33,28 @@ DeviceInfo g_devices[kMaxDevices];
 std::atomic<int> g_fail_setups{0};   // test hook: set-ups to fail on purpose
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_small_m_max{iq::kSmallMMax};
+std::atomic<int> g_tile_n_override{0};   // 0: by token count; else 128 or 256
+std::atomic<int> g_order_override{0};    // 0: by token count; 1 feature-major; 2 token-major
+
+// Tile width and order of the CTA-pair kernel for M tokens.  One head per
+// tile up to 1024 tokens: the two-head tile leaves SMs idle there (at most
+// 4 x 32 tiles for 76 pairs) and its single accumulator serializes each
+// tile's epilogue with the next tile's MMAs.  Token-major order from 16384
+// tokens, where X and the outputs no longer fit in L2.
+constexpr int kNarrowTileMaxTokens = 1024;
+constexpr int kTokenMajorMinTokens = 16384;
+
+int gemm_tile_n(int M) {
+  const int o = g_tile_n_override.load(std::memory_order_relaxed);
+  if (o == 128 || o == 256) return o;
+  return M <= kNarrowTileMaxTokens ? 128 : 256;
+}
+
+int gemm_token_major(int M) {
+  const int o = g_order_override.load(std::memory_order_relaxed);
+  if (o == 1 || o == 2) return o == 2 ? 1 : 0;
+  return M >= kTokenMajorMinTokens ? 1 : 0;
+}
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -130,7 +152,9 @@ iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq,
   a.m_al = (M + 3) / 4 * 4;
   a.num_m_tiles = (M + 127) / 128;
   a.num_m_pairs = (a.num_m_tiles + iq::gemm_pair_size() - 1) / iq::gemm_pair_size();
-  a.num_pair_tiles = a.num_m_pairs * (iq::kQDim / 256);
+  const int tile_n = gemm_tile_n(M);
+  a.num_pair_tiles = a.num_m_pairs * (iq::kQDim / tile_n);
+  a.token_major = gemm_token_major(M);
   a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   a.rope = rope;
   CUtensorMap tm_x, tm_w, tm_q;
@@ -143,15 +167,17 @@ iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq,
     }
     return iq::launch_small_m_rope_hadamard_fp4(tm_x, tm_w, a, fmt, stream) == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
   }
-  // X: this CTA's 128 token rows per K-block; W: one head (128 rows) per
-  // CTA of the pair; Q codes: one head of 128 rows x 64 bytes per store.
+  // X: this CTA's 128 token rows per K-block; W: half of the tile's W rows
+  // per CTA of the pair; Q codes: one head of 128 rows x 64 bytes per store.
   if (!encode_2d_u8(&tm_x, xq, iq::kLatentDim, static_cast<uint64_t>(M), 128, 128) ||
-      !encode_2d_u8(&tm_w, wq, iq::kLatentDim, iq::kQDim, 128, 256 / iq::gemm_pair_size()) ||
+      !encode_2d_u8(&tm_w, wq, iq::kLatentDim, iq::kQDim, 128,
+                    static_cast<uint32_t>(tile_n / iq::gemm_pair_size())) ||
       !encode_2d_u8(&tm_q, q_fp4, iq::kQDim / 2, static_cast<uint64_t>(M), 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) {
     return IQ_ERR_CUDA;
   }
-  return iq::launch_gemm_rope_hadamard_fp4(tm_x, tm_w, tm_q, a, fmt, max_pairs, stream) == cudaSuccess ? IQ_OK
-                                                                                                        : IQ_ERR_CUDA;
+  return iq::launch_gemm_rope_hadamard_fp4(tm_x, tm_w, tm_q, a, tile_n, fmt, max_pairs, stream) == cudaSuccess
+             ? IQ_OK
+             : IQ_ERR_CUDA;
 }
 
 bool valid_format(int fmt) { return fmt == IQ_FP4_MX || fmt == IQ_FP4_MX_OCP || fmt == IQ_FP4_NV; }
@@ -258,6 +284,7 @@ iq_status iq_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t ti
   a.num_m_tiles = M / 128;
   a.num_m_pairs = 1;
   a.num_pair_tiles = iq::kQDim / 256;
+  a.token_major = 0;
   a.timeout_ns = timeout_ns;
   a.rope = rope;
   // The tensor maps are valid descriptors over the workspace (nothing is
@@ -284,6 +311,11 @@ int iq_set_small_m_threshold(int max_tokens) {
 }
 
 int iq_small_m_threshold(void) { return g_small_m_max.load(); }
+
+void iq_set_gemm_tiling(int tile_n, int order) {
+  g_tile_n_override.store(tile_n == 128 || tile_n == 256 ? tile_n : 0);
+  g_order_override.store(order == 1 || order == 2 ? order : 0);
+}
 
 size_t iq_fp8_scale_words(int M, int K) {
   if (M <= 0 || K <= 0) return 0;

@@ -67,35 +67,49 @@ __device__ uint32_t g_iq_status;
 namespace {
 
 constexpr int BM = 128;                          // token rows per CTA (256 per pair)
-constexpr int BN = 256;                          // output features per tile (two heads)
 constexpr int BK = 128;
 constexpr int kPair = 2;
 constexpr uint16_t kPairMask = 0x3;
 constexpr int kStages = 6;
 static_assert(kNumKBlocks == 2 * kStages, "a tile is two passes over the ring (static phases in the MMA loop)");
 constexpr int kABytes = BM * BK;                 // 16 KB: this CTA's token rows
-constexpr int kBBytes = (BN / kPair) * BK;       // 16 KB: this CTA's head of W
-constexpr int kPairStageTx = kPair * (kABytes + kBBytes);   // bytes landing per stage, both CTAs
 constexpr int kNumEpiWarps = 8;
 constexpr int kThreads = (2 + kNumEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = 0;
+constexpr uint32_t kAccCol = 0;                  // accumulators: columns 0..255
 constexpr uint32_t kSfaCol = 256;                // + 8 g, 4 columns each
-constexpr uint32_t kSfbCol = 288;                // + 8 g, 8 columns each (two 128-row halves)
-
-// Shared-memory map (offsets from a 1024-byte aligned base).
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kABytes;
+constexpr uint32_t kSfbCol = 288;                // + 8 g, 4 columns per head of the tile
 constexpr int kSfaWords = kScaleGroups * 128;    // per buffer
-constexpr int kSfbWords = kScaleGroups * 256;
-constexpr int kOffSfa = kOffB + kStages * kBBytes;
-constexpr int kOffSfb = kOffSfa + 2 * kSfaWords * 4;
-constexpr int kOffOut = kOffSfb + 2 * kSfbWords * 4;   // FP4 code staging: [2 heads][128 rows][64 B]
-constexpr int kOutHeadBytes = BM * 64;
-constexpr int kOffBar = kOffOut + 2 * kOutHeadBytes;
-constexpr int kNumBars = 2 * kStages + 4 + 3;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+constexpr int kOutHeadBytes = BM * 64;           // FP4 codes of one head of the CTA's rows
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1;
+
+// Tile width kBN (output features per pair tile): 256 = two heads, each CTA
+// loading 128 W rows (one head) per K-block; 128 = one head, each CTA loading
+// 64 of its rows.  The narrow tile halves the MMA work per tile, so small and
+// mid-size token counts spread over more SMs, and its 128-column accumulator
+// fits twice in tensor memory, so a tile's epilogue overlaps the next tile's
+// MMAs; the wide tile reads each X K-block once for two heads, which halves
+// the X traffic from L2 to the SMs per FLOP at large token counts.
+template <int kBN>
+struct K2Layout {
+  static constexpr int kHeads = kBN / kHeadDim;              // heads per tile
+  static constexpr int kBBytes = (kBN / kPair) * BK;         // this CTA's W rows per K-block
+  static constexpr int kStageTx = kPair * (kABytes + kBBytes);   // bytes landing per stage, both CTAs
+  static constexpr int kAccBufs = kBN == 128 ? 2 : 1;        // accumulators in tensor memory
+  static constexpr int kSfbWords = kScaleGroups * kBN;       // per buffer
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffSfa = kOffB + kStages * kBBytes;
+  static constexpr int kOffSfb = kOffSfa + 2 * kSfaWords * 4;
+  static constexpr int kOffOut = kOffSfb + 2 * kSfbWords * 4;   // FP4 code staging: [heads][128 rows][64 B]
+  static constexpr int kOffBar = kOffOut + kHeads * kOutHeadBytes;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;    // + alignment slack
+  static_assert(kBN == 128 || kBN == 256, "tile width");
+  static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0 && kOffOut % 1024 == 0, "swizzled tiles");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kAccBufs * kBN <= static_cast<int>(kSfaCol), "accumulators below the scale columns");
+};
 
 __device__ __forceinline__ void fail(volatile uint32_t* abort_flag, uint32_t bit) {
   atomicOr(&g_iq_status, bit);
@@ -255,33 +269,37 @@ __device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int hea
 // waits all give up with nothing asynchronous in flight (the only tensor-core
 // work is the scale-factor copy, which completes).  It exercises the give-up
 // and teardown path; the product launches only kNoLoads = false.
-template <int kFmt, bool kNoLoads = false>
+template <int kFmt, int kBN, bool kNoLoads = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_rope_hadamard_fp4_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ GemmArgs args) {
+  using L = K2Layout<kBN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sA = smem + kOffA;
-  uint8_t* sB = smem + kOffB;
-  uint32_t* sSfa = reinterpret_cast<uint32_t*>(smem + kOffSfa);
-  uint32_t* sSfb = reinterpret_cast<uint32_t*>(smem + kOffSfb);
-  uint8_t* sOut = smem + kOffOut;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint8_t* sA = smem + L::kOffA;
+  uint8_t* sB = smem + L::kOffB;
+  uint32_t* sSfa = reinterpret_cast<uint32_t*>(smem + L::kOffSfa);
+  uint32_t* sSfb = reinterpret_cast<uint32_t*>(smem + L::kOffSfb);
+  uint8_t* sOut = smem + L::kOffOut;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* full = bars;                       // leader: both CTAs' loads of a stage landed
   uint64_t* empty = bars + kStages;            // both: the pair's MMAs released a stage
   uint64_t* sf_full = bars + 2 * kStages;      // leader: both CTAs staged a tile's scales
   uint64_t* sf_empty = sf_full + 2;            // both: the scale copies completed
-  uint64_t* tmem_full = sf_empty + 2;          // both: the tile's accumulator is complete
-  uint64_t* tmem_empty = tmem_full + 1;        // leader: both CTAs drained the accumulator
-  uint64_t* final_bar = tmem_empty + 1;        // both: every pair MMA has completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
+  uint64_t* tmem_full = sf_empty + 2;          // both: accumulator b holds a complete tile
+  uint64_t* tmem_empty = tmem_full + 2;        // leader: both CTAs drained accumulator b
+  uint64_t* final_bar = tmem_empty + 2;        // both: every pair MMA has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t timeout = args.timeout_ns;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
+  // Epilogue warps that read the accumulator: four per head of the tile (one
+  // per 32-lane quarter of tensor memory).
+  constexpr int kDrainWarps = 4 * L::kHeads;
 
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_x);
@@ -294,9 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sf_full[b], kPair);
       mbar_init(&sf_empty[b], 1);
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], kPair * kDrainWarps);
     }
-    mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, kPair * kNumEpiWarps);
     mbar_init(final_bar, 1);
     *abort_flag = 0u;
     fence_mbar_init();
@@ -319,20 +337,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Leader-CTA addresses of the barriers that collect the pair's work.
   const uint32_t full_leader0 = mapa_shared(smem_u32(&full[0]), 0);
   const uint32_t sf_full_leader0 = mapa_shared(smem_u32(&sf_full[0]), 0);
-  const uint32_t tmem_empty_leader = mapa_shared(smem_u32(tmem_empty), 0);
+  const uint32_t tmem_empty_leader0 = mapa_shared(smem_u32(&tmem_empty[0]), 0);
 
-  // Pair tile pt: token rows [256 * (pt % num_m_pairs), +256) split by CTA
-  // rank, features [256 * (pt / num_m_pairs), +256).  Each pair takes a
-  // contiguous run of tiles, so consecutive tiles mostly share the same two
-  // heads: their W tiles stay hot in L2 and their weight scales are staged
-  // and copied into tensor memory only when the heads change.
+  // Pair tile pt covers token rows [256 mp, +256) (split by CTA rank) and
+  // features [kBN n, +kBN).  Each pair takes a contiguous run of tiles.  In
+  // feature-major order (mp = pt % num_m_pairs) consecutive tiles share their
+  // heads: W stays hot in L2 and the weight scales are staged and copied
+  // into tensor memory only when the heads change.  In token-major order
+  // (mp = pt / n_tiles) consecutive tiles share their token rows, so the pairs
+  // running at one time read few distinct X row blocks, each from HBM once,
+  // while W (12.6 MB) stays in L2: the order for token counts whose X and
+  // outputs do not fit in L2.
+  constexpr int n_tiles = kQDim / kBN;
   const int num_pairs = static_cast<int>(cluster_count_x());
   const int tiles_per_pair = (args.num_pair_tiles + num_pairs - 1) / num_pairs;
   const int first_pt = static_cast<int>(cluster_id_x()) * tiles_per_pair;
   const int end_pt = min(first_pt + tiles_per_pair, args.num_pair_tiles);
   const int num_m_pairs = args.num_m_pairs;
-  auto tile_m0 = [&](int pt) { return ((pt % num_m_pairs) * kPair + static_cast<int>(rank)) * BM; };
-  auto tile_n = [&](int pt) { return pt / num_m_pairs; };
+  const bool token_major = args.token_major != 0;
+  auto tile_mp = [&](int pt) { return token_major ? pt / n_tiles : pt % num_m_pairs; };
+  auto tile_n = [&](int pt) { return token_major ? pt % n_tiles : pt / num_m_pairs; };
+  auto tile_m0 = [&](int pt) { return (tile_mp(pt) * kPair + static_cast<int>(rank)) * BM; };
   auto new_heads = [&](int pt) { return pt == first_pt || tile_n(pt - 1) != tile_n(pt); };
 
   if (warp == 0) {
@@ -342,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The next tile's scale words are fetched into registers while the
     // current tile's K-blocks stream, so no global-load latency sits at a
     // tile boundary.  ra: this lane's 4 rows x 3 groups of activation-scale
-    // words; rb: the two heads' weight-scale words per group.
-    uint32_t ra[kScaleGroups][4], rb[kScaleGroups][2];
+    // words; rb: the tile's heads' weight-scale words per group.
+    uint32_t ra[kScaleGroups][4], rb[kScaleGroups][L::kHeads];
     auto fetch_scales = [&](int pt) {
       if (pt >= end_pt) return;
       const int m0 = tile_m0(pt);
@@ -357,10 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (new_heads(pt)) {
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint8_t* ws = args.w_sf + (n_tile * 2 + half) * kNumKBlocks + 4 * g;
-            rb[g][half] = static_cast<uint32_t>(__ldg(ws)) | (static_cast<uint32_t>(__ldg(ws + 1)) << 8) |
-                          (static_cast<uint32_t>(__ldg(ws + 2)) << 16) | (static_cast<uint32_t>(__ldg(ws + 3)) << 24);
+          for (int h = 0; h < L::kHeads; ++h) {
+            const uint8_t* ws = args.w_sf + (n_tile * L::kHeads + h) * kNumKBlocks + 4 * g;
+            rb[g][h] = static_cast<uint32_t>(__ldg(ws)) | (static_cast<uint32_t>(__ldg(ws + 1)) << 8) |
+                       (static_cast<uint32_t>(__ldg(ws + 2)) << 16) | (static_cast<uint32_t>(__ldg(ws + 3)) << 24);
           }
         }
       }
@@ -380,19 +405,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Scale factors in the tcgen05.cp 32x128b layout: word [r * 4 + c] of a
       // 128-row tile holds row c * 32 + r.  SFA: this CTA's 128 token rows;
-      // SFB: both heads of the tile (all 256 rows), staged only when the heads
-      // differ from the previous tile's (the MMA issuer copies it only then).
+      // SFB: the tile's heads (128 rows each, all of them in both CTAs),
+      // staged only when the heads differ from the previous tile's (the MMA
+      // issuer copies it only then).
       uint32_t* sfa = sSfa + buf * kSfaWords;
-      uint32_t* sfb = sSfb + buf * kSfbWords;
+      uint32_t* sfb = sSfb + buf * L::kSfbWords;
       const bool stage_sfb = new_heads(pt);
 #pragma unroll
       for (int g = 0; g < kScaleGroups; ++g) {
         *reinterpret_cast<uint4*>(sfa + g * 128 + lane * 4) = make_uint4(ra[g][0], ra[g][1], ra[g][2], ra[g][3]);
         if (stage_sfb) {
 #pragma unroll
-          for (int half = 0; half < 2; ++half)
-            *reinterpret_cast<uint4*>(sfb + g * 256 + half * 128 + lane * 4) =
-                make_uint4(rb[g][half], rb[g][half], rb[g][half], rb[g][half]);
+          for (int h = 0; h < L::kHeads; ++h)
+            *reinterpret_cast<uint4*>(sfb + g * kBN + h * 128 + lane * 4) =
+                make_uint4(rb[g][h], rb[g][h], rb[g][h], rb[g][h]);
         }
       }
       fence_proxy_async_smem();
@@ -408,11 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if constexpr (!kNoLoads) {
-            if (leader) mbar_arrive_expect_tx(&full[stage], kPairStageTx);
+            if (leader) mbar_arrive_expect_tx(&full[stage], L::kStageTx);
             const uint32_t bar = full_leader0 + 8u * stage;
             tma_load_2d_pair(sA + stage * kABytes, &tm_x, bar, kb * BK, m0);
-            tma_load_2d_pair(sB + stage * kBBytes, &tm_w, bar, kb * BK,
-                             n_tile * BN + static_cast<int>(rank) * (BN / kPair));
+            tma_load_2d_pair(sB + stage * L::kBBytes, &tm_w, bar, kb * BK,
+                             n_tile * kBN + static_cast<int>(rank) * (kBN / kPair));
             issued_mask |= 1u << stage;
             issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           }
@@ -427,7 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Teardown: this CTA's loads signal the leader's barriers, so their
     // landing is observed through the stage's release by the pair's MMAs,
-    // which consumed them.
+    // which consumed them.  The teardown waits get twice the limit (see the
+    // final-commit wait below).
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s) {
         if ((issued_mask >> s) & 1u) {
@@ -444,28 +471,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         const uint64_t adesc0 = smem_desc_sw128(smem_u32(sA));
         const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sB));
-        const uint32_t idesc0 = idesc_mxf8_e4m3(kPair * BM, BN, 0, 0);
+        const uint32_t idesc0 = idesc_mxf8_e4m3(kPair * BM, kBN, 0, 0);
         for (int pt = first_pt; pt < end_pt && ok; ++pt, ++local) {
           if (*abort_flag) break;
           const int buf = local & 1;
+          const int acc = local % L::kAccBufs;
           if (!mbar_wait(&sf_full[buf], (local >> 1) & 1, timeout) ||
-              !mbar_wait(tmem_empty, (local & 1) ^ 1, timeout)) {
+              !mbar_wait(&tmem_empty[acc], ((local / L::kAccBufs) & 1) ^ 1, timeout)) {
             fail(abort_flag, kStatusMmaWait);
             break;
           }
           tc_fence_after_sync();
           const uint32_t* sfa = sSfa + buf * kSfaWords;
-          const uint32_t* sfb = sSfb + buf * kSfbWords;
+          const uint32_t* sfb = sSfb + buf * L::kSfbWords;
           const bool copy_sfb = new_heads(pt);
 #pragma unroll
           for (int g = 0; g < kScaleGroups; ++g) {
             tc_cp_32x128b_warpx4_pair(tmem + kSfaCol + 8 * g, smem_desc_sf(smem_u32(sfa + g * 128)));
             if (copy_sfb) {
-              tc_cp_32x128b_warpx4_pair(tmem + kSfbCol + 8 * g, smem_desc_sf(smem_u32(sfb + g * 256)));
-              tc_cp_32x128b_warpx4_pair(tmem + kSfbCol + 8 * g + 4, smem_desc_sf(smem_u32(sfb + g * 256 + 128)));
+#pragma unroll
+              for (int h = 0; h < L::kHeads; ++h)
+                tc_cp_32x128b_warpx4_pair(tmem + kSfbCol + 8 * g + 4 * h,
+                                          smem_desc_sf(smem_u32(sfb + g * kBN + h * 128)));
             }
           }
           tc_commit_pair(&sf_empty[buf], kPairMask);
+          const uint32_t d_tmem = tmem + kAccCol + static_cast<uint32_t>(acc * kBN);
           // The K loop does little between MMAs: a tile is exactly two
           // passes over the ring, so every stage index, barrier phase, scale
           // ID and descriptor offset below is a compile-time constant and the
@@ -481,19 +512,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             const uint64_t adesc = adesc0 + static_cast<uint64_t>(s * (kABytes >> 4));
-            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(s * (kBBytes >> 4));
+            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(s * (L::kBBytes >> 4));
             const uint32_t sfid = static_cast<uint32_t>(kb & 3);
             const uint32_t idesc = idesc0 | (sfid << 4) | (sfid << 29);
             const uint32_t sf_off = 8u * static_cast<uint32_t>(kb >> 2);
 #pragma unroll
             for (int k = 0; k < BK / 32; ++k) {
               // advance 32 bytes along K inside the 128-byte swizzle atom
-              tc_mma_mxf8_pair(tmem + kAccCol, adesc + 2 * k, bdesc + 2 * k, idesc, tmem + kSfaCol + sf_off,
+              tc_mma_mxf8_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, tmem + kSfaCol + sf_off,
                                tmem + kSfbCol + sf_off, (kb | k) != 0);
             }
             tc_commit_pair(&empty[s], kPairMask);   // frees the stage in both CTAs
           }
-          if (ok) tc_commit_pair(tmem_full, kPairMask);
+          if (ok) tc_commit_pair(&tmem_full[acc], kPairMask);
         }
         tc_commit_pair(final_bar, kPairMask);
       }
@@ -509,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;            // the TMEM lane group this warp may read
     const int half = (warp - 2) >> 2;     // which head of the tile
+    const bool drains = half < L::kHeads; // warp-uniform: this warp has a head in every tile
     const int trow = quad * 32 + lane;    // row within the CTA's 128-row tile
     uint8_t* stage_row = sOut + half * kOutHeadBytes + trow * 64;
     const int swz = (trow >> 1) & 3;
@@ -516,43 +548,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     int local = 0;
     for (int pt = first_pt; pt < end_pt; ++pt, ++local) {
       const int row = tile_m0(pt) + trow;
-      const int head = tile_n(pt) * 2 + half;
-      const int pos = row < args.M ? static_cast<int>(ld_dependent_u32(args.pos + row)) : 0;   // in flight during the wait
+      const int head = tile_n(pt) * L::kHeads + half;
+      const int acc = local % L::kAccBufs;
+      const int pos = drains && row < args.M ? static_cast<int>(ld_dependent_u32(args.pos + row)) : 0;   // in flight during the wait
       // The previous tile's bulk stores must have read the staging tile
       // before anyone overwrites it.
       if (store_issuer) tma_store_wait_read();
-      const bool got = mbar_wait(tmem_full, local & 1, timeout);
-      if (!got) fail(abort_flag, kStatusEpilogueWait);
+      bool got = true;
+      if (drains) {
+        got = mbar_wait(&tmem_full[acc], (local / L::kAccBufs) & 1, timeout);
+        if (!got) fail(abort_flag, kStatusEpilogueWait);
+      }
       // One decision for all epilogue warps (they meet at a named barrier
       // below); this barrier also tells them the staging tile is free.
       if (!named_barrier_and(1, kNumEpiWarps * 32, got && *abort_flag == 0u)) break;
-      tc_fence_after_sync();
-      float v[128];
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kAccCol + half * 128;
-      tmem_ld_32x32b_x32(taddr + 0, v + 0);
-      tmem_ld_32x32b_x32(taddr + 32, v + 32);
-      tmem_ld_32x32b_x32(taddr + 64, v + 64);
-      tmem_ld_32x32b_x32(taddr + 96, v + 96);
-      tmem_ld_wait(v + 0);
-      tmem_ld_wait(v + 32);
-      tmem_ld_wait(v + 64);
-      tmem_ld_wait(v + 96);
-      tc_fence_before_sync();
-      __syncwarp();
-      // The accumulator values are in registers (tcgen05.wait::ld above), so
-      // the leader may overwrite it: a CTA-scope arrive suffices and does not
-      // wait for earlier global stores to reach L2.
-      if (lane == 0) mbar_arrive_remote(tmem_empty_leader);
-      uint64_t p[64];
+      if (drains) {
+        tc_fence_after_sync();
+        float v[128];
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kAccCol +
+                               static_cast<uint32_t>(acc * kBN + half * 128);
+        tmem_ld_32x32b_x32(taddr + 0, v + 0);
+        tmem_ld_32x32b_x32(taddr + 32, v + 32);
+        tmem_ld_32x32b_x32(taddr + 64, v + 64);
+        tmem_ld_32x32b_x32(taddr + 96, v + 96);
+        tmem_ld_wait(v + 0);
+        tmem_ld_wait(v + 32);
+        tmem_ld_wait(v + 64);
+        tmem_ld_wait(v + 96);
+        tc_fence_before_sync();
+        __syncwarp();
+        // The accumulator values are in registers (tcgen05.wait::ld above), so
+        // the leader may overwrite it: a CTA-scope arrive suffices and does not
+        // wait for earlier global stores to reach L2.
+        if (lane == 0) mbar_arrive_remote(tmem_empty_leader0 + 8u * static_cast<uint32_t>(acc));
+        uint64_t p[64];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) p[j] = f2_pack(v[2 * j], v[2 * j + 1]);
-      if (row < args.M) epilogue_row<kFmt>(p, row, head, pos, args, stage_row, swz);
+        for (int j = 0; j < 64; ++j) p[j] = f2_pack(v[2 * j], v[2 * j + 1]);
+        if (row < args.M) epilogue_row<kFmt>(p, row, head, pos, args, stage_row, swz);
+      }
       fence_proxy_async_smem();
       named_barrier_sync(1, kNumEpiWarps * 32);
       if (store_issuer) {
         // Rows past M are clipped by the bulk store.
-        tma_store_2d(&tm_q, sOut, tile_n(pt) * 2 * 64, tile_m0(pt));
-        tma_store_2d(&tm_q, sOut + kOutHeadBytes, (tile_n(pt) * 2 + 1) * 64, tile_m0(pt));
+#pragma unroll
+        for (int h = 0; h < L::kHeads; ++h)
+          tma_store_2d(&tm_q, sOut + h * kOutHeadBytes, (tile_n(pt) * L::kHeads + h) * 64, tile_m0(pt));
         tma_store_commit();
       }
     }
@@ -573,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // scheduled while the preceding kernel of the stream (the quantizer) runs;
 // it waits for that kernel's completion (griddepcontrol.wait) before any
 // global memory access.
-cudaLaunchConfig_t pair_config(int pairs, cudaLaunchAttribute* attr, cudaStream_t stream) {
+cudaLaunchConfig_t pair_config(int pairs, int smem_bytes, cudaLaunchAttribute* attr, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kPair;
   attr[0].val.clusterDim.y = 1;
@@ -583,53 +623,76 @@ cudaLaunchConfig_t pair_config(int pairs, cudaLaunchAttribute* attr, cudaStream_
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pairs * kPair, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cfg;
 }
 
-}  // namespace
+template <int kFmt, int kBN, bool kNoLoads = false>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(gemm_rope_hadamard_fp4_kernel<kFmt, kBN, kNoLoads>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, K2Layout<kBN>::kSmemBytes);
+}
 
-int gemm_smem_bytes() { return kSmemBytes; }
+template <int kFmt, int kBN, bool kNoLoads = false>
+cudaError_t launch_one(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
+                       const GemmArgs& args, int pairs, cudaStream_t stream) {
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pair_config(pairs, K2Layout<kBN>::kSmemBytes, attr, stream);
+  return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel<kFmt, kBN, kNoLoads>, tm_x, tm_w, tm_q, args);
+}
+
+// Pairs to launch: at most max_pairs, and no more than the tiles need once
+// each pair takes ceil(tiles / pairs) of them.
+int launch_pairs(int tiles, int max_pairs) {
+  const int p = tiles < max_pairs ? tiles : max_pairs;
+  const int per = (tiles + p - 1) / p;
+  return (tiles + per - 1) / per;
+}
+
+}  // namespace
 
 int gemm_pair_size() { return kPair; }
 
 cudaError_t gemm_setup_device(int* max_pairs) {
-  for (const void* fn : {reinterpret_cast<const void*>(gemm_rope_hadamard_fp4_kernel<kFp4Mx>),
-                         reinterpret_cast<const void*>(gemm_rope_hadamard_fp4_kernel<kFp4MxOcp>),
-                         reinterpret_cast<const void*>(gemm_rope_hadamard_fp4_kernel<kFp4Nv>)}) {
-    const cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  for (cudaError_t err : {set_smem_attr<kFp4Mx, 256>(), set_smem_attr<kFp4MxOcp, 256>(), set_smem_attr<kFp4Nv, 256>(),
+                          set_smem_attr<kFp4Mx, 128>(), set_smem_attr<kFp4MxOcp, 128>(), set_smem_attr<kFp4Nv, 128>(),
+                          set_smem_attr<kFp4Mx, 256, true>()}) {
     if (err != cudaSuccess) return err;
   }
+  // One CTA per SM for either width (tensor memory and registers), so the
+  // wide instance's occupancy holds for both.
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = pair_config(1, attr, nullptr);
-  return cudaOccupancyMaxActiveClusters(max_pairs, gemm_rope_hadamard_fp4_kernel<kFp4Mx>, &cfg);
+  const cudaLaunchConfig_t cfg = pair_config(1, K2Layout<256>::kSmemBytes, attr, nullptr);
+  return cudaOccupancyMaxActiveClusters(max_pairs, gemm_rope_hadamard_fp4_kernel<kFp4Mx, 256>, &cfg);
 }
 
 cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
-                                          const GemmArgs& args, int fp4_format, int max_pairs, cudaStream_t stream) {
-  const int pairs = args.num_pair_tiles < max_pairs ? args.num_pair_tiles : max_pairs;
-  cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = pair_config(pairs, attr, stream);
+                                          const GemmArgs& args, int tile_n, int fp4_format, int max_pairs,
+                                          cudaStream_t stream) {
+  const int pairs = launch_pairs(args.num_pair_tiles, max_pairs);
+  if (tile_n == 128) {
+    switch (fp4_format) {
+      case kFp4Mx: return launch_one<kFp4Mx, 128>(tm_x, tm_w, tm_q, args, pairs, stream);
+      case kFp4MxOcp: return launch_one<kFp4MxOcp, 128>(tm_x, tm_w, tm_q, args, pairs, stream);
+      case kFp4Nv: return launch_one<kFp4Nv, 128>(tm_x, tm_w, tm_q, args, pairs, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (tile_n != 256) return cudaErrorInvalidValue;
   switch (fp4_format) {
-    case kFp4Mx: return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel<kFp4Mx>, tm_x, tm_w, tm_q, args);
-    case kFp4MxOcp: return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel<kFp4MxOcp>, tm_x, tm_w, tm_q, args);
-    case kFp4Nv: return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel<kFp4Nv>, tm_x, tm_w, tm_q, args);
+    case kFp4Mx: return launch_one<kFp4Mx, 256>(tm_x, tm_w, tm_q, args, pairs, stream);
+    case kFp4MxOcp: return launch_one<kFp4MxOcp, 256>(tm_x, tm_w, tm_q, args, pairs, stream);
+    case kFp4Nv: return launch_one<kFp4Nv, 256>(tm_x, tm_w, tm_q, args, pairs, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_gemm_wait_selftest(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
                                       const GemmArgs& args, int max_pairs, cudaStream_t stream) {
-  const cudaError_t err = cudaFuncSetAttribute(gemm_rope_hadamard_fp4_kernel<kFp4Mx, true>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (err != cudaSuccess) return err;
-  const int pairs = args.num_pair_tiles < max_pairs ? args.num_pair_tiles : max_pairs;
-  cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = pair_config(pairs, attr, stream);
-  return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel<kFp4Mx, true>, tm_x, tm_w, tm_q, args);
+  return launch_one<kFp4Mx, 256, true>(tm_x, tm_w, tm_q, args, launch_pairs(args.num_pair_tiles, max_pairs), stream);
 }
 
 cudaError_t read_device_status(uint32_t* flags, bool reset) {

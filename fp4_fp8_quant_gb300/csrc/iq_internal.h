@@ -55,7 +55,8 @@ struct GemmArgs {
   int m_al;
   int num_m_tiles;
   int num_m_pairs;       // ceil(num_m_tiles / 2): 256-token row blocks of a CTA pair
-  int num_pair_tiles;    // num_m_pairs * 32 feature tiles of 256
+  int num_pair_tiles;    // num_m_pairs * (8192 / tile width) pair tiles
+  int token_major;       // pair-tile order: 0 feature-major, 1 token-major
   unsigned long long timeout_ns;
   RopeTurns rope;
 };
@@ -81,11 +82,13 @@ cudaError_t launch_quant_1x128_host_rows(const void* x, int M, int K, long long 
 // Kernel attribute set-up of the fused GEMM on the current device; returns
 // how many of its CTA pairs fit on the device at once.
 cudaError_t gemm_setup_device(int* max_pairs);
-int gemm_smem_bytes();
 int gemm_pair_size();
 
+// tile_n: output features per pair tile, 256 (two heads) or 128 (one head);
+// the W tensor map's box is tile_n / 2 rows.
 cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
-                                          const GemmArgs& args, int fp4_format, int max_pairs, cudaStream_t stream);
+                                          const GemmArgs& args, int tile_n, int fp4_format, int max_pairs,
+                                          cudaStream_t stream);
 
 // The fused GEMM kernel's wait self-test instance (no TMA loads: every wait
 // that depends on them gives up after args.timeout_ns).

@@ -43,6 +43,7 @@ SIGNATURES = {
     "iq_prepare_q_static": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
     "iq_set_small_m_threshold": (_I, [_I]),
     "iq_small_m_threshold": (_I, []),
+    "iq_set_gemm_tiling": (None, [_I, _I]),
     "iq_fp4_scale_bytes": (_SZ, [_I]),
     "iq_prepare_q_ex": (_I, [_P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
     "iq_prepare_q_host_workspace": (_SZ, [_I, _I]),
@@ -284,6 +285,13 @@ def device_status(reset: bool = False) -> int:
     if code not in (0, -7):
         raise IQError(code, "iq_device_status")
     return int(v.value)
+
+
+def set_gemm_tiling(tile_n: int = 0, order: int = 0) -> None:
+    """Tuning override of the CTA-pair kernel's tiling (include/iq.h,
+    iq_set_gemm_tiling): tile_n 128 or 256, order 1 feature-major or 2
+    token-major; 0 restores the default."""
+    lib().iq_set_gemm_tiling(int(tile_n), int(order))
 
 
 def set_wait_timeout_ns(ns: int) -> None:

@@ -119,6 +119,16 @@ int iq_set_small_m_threshold(int max_tokens);
 /* The current threshold (see iq_set_small_m_threshold). */
 int iq_small_m_threshold(void);
 
+/* Tuning override of the CTA-pair kernel's tiling, for measurements.  By
+ * default the kernel takes one head (128 output features) per pair tile for
+ * M <= 1024 and two heads (256) above, and orders the pair tiles
+ * feature-major below 16384 tokens and token-major from there.  tile_n: 128
+ * or 256 forces that width, any other value restores the default; order: 1
+ * forces feature-major, 2 token-major, any other value restores the default.
+ * Results are the same under every setting (the same sums in the same order
+ * per output).  Process-wide; applies to later calls. */
+void iq_set_gemm_tiling(int tile_n, int order);
+
 /* ------------------------------------------------------------------------
  * 1. FP8 1x128 quantizer with packed UE8M0 scales.
  * ------------------------------------------------------------------------ */
