@@ -5,11 +5,14 @@ call on the BF16 latent [4632, 1536] -- the FP8 1x128 quantizer, then the
 fused block-scaled FP8 GEMM with the RoPE -> Hadamard -> FP4 epilogue
 (launched as the quantizer's programmatic dependent), producing packed FP4 Q
 [4632, 4096] and its UE8M0 scales [4632, 256].  Inputs are seeded
-synthetic data resident in HBM before the timed region; L2 is flushed (256 MB written, then 256 MB read, so no dirty
-lines are left for the timed kernels to write back) between timed steps,
-outside the CUDA-event intervals.  `value` is the token count over the median
-of the K event-timed steps (mean, minimum and maximum are reported beside it);
-the warm-up runs at least W steps and at least half a second.  Also measured in the same run: the quantizer alone on
+synthetic data resident in HBM before the timed region; L2 is flushed (256 MB
+written, then 256 MB read, so no dirty lines are left for the timed kernels to
+write back) between timed steps, outside the CUDA-event intervals.  `value` is
+the token count over the median of the K event-timed steps (mean, minimum and
+maximum are reported beside it); the warm-up runs at least W steps and at
+least half a second.  The steady state of steps run back to back over
+rotating buffer sets (total over twice the L2 size; each step then also
+writes back the outputs of earlier steps) is reported as `back_to_back`.  Also measured in the same run: the quantizer alone on
 BF16 [4632, 7168] (GB/s against HBM), the GEMM's own launch time (for the
 roofline), the end-to-end call iq_prepare_q_host on page-locked host
 buffers (the latent read from and the FP4 output written to host memory
@@ -315,75 +318,128 @@ def run_ours(args):
         flush_buf.fill_(rank & 0xFF)
         flush_src.sum()
 
+    # Rotating buffer sets.  A timed run cycles through sets of inputs,
+    # outputs and workspace whose total exceeds twice the L2 size, so every
+    # step reads data that is not in L2 (each set was last touched several
+    # steps before) while the steps run back to back, as repeated calls do.
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    def sets_for(bytes_per_set):
+        return max(2, -(-2 * l2_bytes // bytes_per_set) + 1)
+
+    def time_back_to_back(fns, steps, warmup):
+        """Runs fns[i % len(fns)] for i < warmup untimed, then `steps` times
+        back to back with an event between consecutive steps; returns the
+        per-step intervals (ms) and the total (ms)."""
+        n = len(fns)
+        for i in range(warmup):
+            fns[i % n]()
+        torch.cuda.synchronize()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        evs[0].record(stream)
+        for i in range(steps):
+            fns[i % n]()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+        return per, evs[0].elapsed_time(evs[-1])
+
     # ---------------------------------------------------- the prefill chain
     x, wq, wsf, pos = W.prefill_chain(M_PREFILL)
-    lat = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
-    w = torch.from_numpy(wq).to(dev)
-    ws = torch.from_numpy(wsf).to(dev)
-    p = torch.from_numpy(pos).to(dev)
     M = M_PREFILL
-    xq = torch.empty((M, K_LATENT), dtype=torch.uint8, device=dev)
-    xs = torch.empty((3, (M + 3) // 4 * 4), dtype=torch.int32, device=dev)
-    q = torch.empty((M, N_Q // 2), dtype=torch.uint8, device=dev)
-    s = torch.empty((M, N_Q // 32), dtype=torch.uint8, device=dev)
-    work = torch.empty(iq.prepare_q_workspace_bytes(M), dtype=torch.uint8, device=dev)
+    lat0 = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+    w0 = torch.from_numpy(wq).to(dev)
+    ws = torch.from_numpy(wsf).to(dev)
+    p0 = torch.from_numpy(pos).to(dev)
+    ws_bytes = iq.prepare_q_workspace_bytes(M)
+    set_bytes = lat0.numel() * 2 + w0.numel() + p0.numel() * 4 + M * (N_Q // 2 + N_Q // 32) + ws_bytes
+    n_sets = sets_for(set_bytes)
+    chain_sets = []
+    for i in range(n_sets):
+        chain_sets.append({"lat": lat0.clone(), "w": w0.clone(), "p": p0.clone(),
+                           "q": torch.empty((M, N_Q // 2), dtype=torch.uint8, device=dev),
+                           "s": torch.empty((M, N_Q // 32), dtype=torch.uint8, device=dev),
+                           "work": torch.empty(ws_bytes, dtype=torch.uint8, device=dev),
+                           "xq": torch.empty((M, K_LATENT), dtype=torch.uint8, device=dev),
+                           "xs": torch.empty((3, (M + 3) // 4 * 4), dtype=torch.int32, device=dev)})
 
-    def step():
+    def step_fn(c, fmt="mx", q=None, s=None):
         # iq_prepare_q: the quantizer, then the fused GEMM as its programmatic
         # dependent (no host or event work between the two launches).
-        iq.prepare_q(lat, w, ws, p, q_fp4=q, q_sf=s, workspace=work)
+        return lambda: iq.prepare_q(c["lat"], c["w"], ws, c["p"], q_fp4=c["q"] if q is None else q,
+                                    q_sf=c["s"] if s is None else s, workspace=c["work"], fp4_format=fmt)
 
+    steps = [step_fn(c) for c in chain_sets]
     # The clock sampler starts before the warm-up, so its start-up and the
     # clocks' ramp from idle both fall before the timed steps.  The warm-up is
-    # at least W steps (each after an L2 flush, as timed) and at least
-    # WARMUP_MIN_S of them.
+    # at least W steps and at least WARMUP_MIN_S of them.
     clocks = ClockSampler(local).__enter__()
     t0 = time.perf_counter()
     n_warm = 0
     while n_warm < max(3, args.warmup) or time.perf_counter() - t0 < WARMUP_MIN_S:
-        flush_l2()
-        step()
+        steps[n_warm % n_sets]()
         n_warm += 1
-        if n_warm % 16 == 0:
+        if n_warm % 64 == 0:
             torch.cuda.synchronize()
+    # Timed steps: each after an L2 flush (256 MB written, then 256 MB read,
+    # so that no dirty lines of earlier work are left for the step to write
+    # back), outside the event interval; the GPU is idle when the step is
+    # launched, so the launch latency of both kernels is inside it.
     barrier()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    barrier()
     t_wall = time.perf_counter()
     for i in range(args.steps):
         flush_l2()
         ev[i][0].record(stream)
-        step()
+        steps[i % n_sets]()
         ev[i][1].record(stream)
     barrier()
     t_wall = time.perf_counter() - t_wall
-    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    step_ms = [a.elapsed_time(b) for a, b in ev]
     ms_per_step = max_over_ranks(statistics.median(step_ms), world, dev)
     value = whole_job_rate(M, world, ms_per_step)
     step_stats = {"median_ms": statistics.median(step_ms), "mean_ms": sum(step_ms) / len(step_ms),
                   "min_ms": min(step_ms), "max_ms": max(step_ms), "warmup_steps_run": n_warm}
 
-    # The fused GEMM's own launch duration (for the roofline): the same
-    # launches with events around the GEMM alone (the quantizer runs first,
-    # outside the interval; W is not in L2, the FP8 latent is, as in a step).
-    k2ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for a, b in k2ev:
-        flush_l2()
-        iq.fp8_quant_1x128_ue8m0(lat, y=xq, scales=xs)
-        a.record(stream)
-        iq.gemm_rope_hadamard_fp4(xq, xs, w, ws, p, q_fp4=q, q_sf=s)
-        b.record(stream)
-    torch.cuda.synchronize()
-    k2_ms = [a.elapsed_time(b) for a, b in k2ev]
+    # Steady state: the same steps back to back over the rotating sets.  Each
+    # step then also writes back the dirty outputs of the steps before it
+    # (the flush above moves that outside the timed interval).
+    bb_ms, bb_total = time_back_to_back(steps, args.steps, n_sets)
+    back_to_back = {"median_ms": statistics.median(bb_ms), "mean_ms": bb_total / len(bb_ms),
+                    "tokens_per_s": M / (bb_total / len(bb_ms) * 1e-3), "buffer_sets": n_sets,
+                    "bytes_per_set": set_bytes,
+                    "how": f"steps back to back over {n_sets} rotating buffer sets (more than twice L2)"}
+
+    # The fused GEMM's own launch duration (for the roofline): per timed
+    # launch an L2 flush, then the quantizer (outside the interval), then the
+    # GEMM between events (W from HBM, the FP8 latent in L2, as in a step).
+    def flushed_ms(pre, fn, n):
+        out = []
+        for i in range(n):
+            flush_l2()
+            if pre is not None:
+                pre(i)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn(i)
+            b.record(stream)
+            out.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in out]
+
+    def k1_of(i):
+        c = chain_sets[i % n_sets]
+        iq.fp8_quant_1x128_ue8m0(c["lat"], y=c["xq"], scales=c["xs"])
+
+    def k2_of(i):
+        c = chain_sets[i % n_sets]
+        iq.gemm_rope_hadamard_fp4(c["xq"], c["xs"], c["w"], ws, c["p"], q_fp4=c["q"], q_sf=c["s"])
+
+    k2_ms = flushed_ms(k1_of, k2_of, args.steps)
     k2_avg_ms = sum(k2_ms) / len(k2_ms)
-    k1ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for a, b in k1ev:
-        flush_l2()
-        a.record(stream)
-        iq.fp8_quant_1x128_ue8m0(lat, y=xq, scales=xs)
-        b.record(stream)
-    torch.cuda.synchronize()
-    k1_avg_ms = sum(a.elapsed_time(b) for a, b in k1ev) / len(k1ev)
+    k1_ms = flushed_ms(None, k1_of, args.steps)
+    k1_avg_ms = sum(k1_ms) / len(k1_ms)
+    k2_bb, k2_bb_total = time_back_to_back([lambda i=i: k2_of(i) for i in range(n_sets)], args.steps, 2 * n_sets)
 
     hbm_peak, bf16_peak, peak_kind = load_peaks()
     fp8_peak_tflops = bf16_peak * FP8_OVER_BF16
@@ -394,6 +450,8 @@ def run_ours(args):
                 "traffic": kernel_traffic("gemm_rope_hadamard_fp4_kernel"),
                 "peak_source": f"{peak_kind} bf16 x {FP8_OVER_BF16:g} (FP8/BF16 nominal ratio)",
                 "avg_launch_ms": k2_avg_ms, "median_launch_ms": statistics.median(k2_ms),
+                "launches": "each after an L2 flush and the quantizer, events around the GEMM alone",
+                "back_to_back_avg_launch_ms": k2_bb_total / len(k2_bb),
                 "flops_per_launch": M * FLOPS_PER_TOKEN,
                 "frac_of_nominal_fp8": achieved_tflops / NOMINAL_FP8_TFLOPS,
                 "cublas_fp8_tflops_same_run": cublas_fp8,
@@ -401,49 +459,51 @@ def run_ours(args):
 
     # ------------------------------------- FP4 output variants (prefill step)
     # The same step with each FP4 output variant of iq_prepare_q_ex (L2
-    # flushed before every step, 50 steps each).
+    # flushed before each timed step).
     fp4_formats = {}
     for fmt in ("mx", "mx_ocp", "nv"):
-        q_f = torch.empty((M, N_Q // 2), dtype=torch.uint8, device=dev)
-        s_f = torch.empty((M, iq.fp4_scale_bytes(fmt)), dtype=torch.uint8, device=dev)
-        for _ in range(3):
-            iq.prepare_q(lat, w, ws, p, q_fp4=q_f, q_sf=s_f, workspace=work, fp4_format=fmt)
-        fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
-        for a, b in fev:
-            flush_l2()
-            a.record(stream)
-            iq.prepare_q(lat, w, ws, p, q_fp4=q_f, q_sf=s_f, workspace=work, fp4_format=fmt)
-            b.record(stream)
-        torch.cuda.synchronize()
-        f_ms = sum(a.elapsed_time(b) for a, b in fev) / len(fev)
-        fp4_formats[fmt] = {"us_per_step": f_ms * 1e3, "tokens_per_s": M / (f_ms * 1e-3),
+        fns = []
+        for c in chain_sets:
+            s_f = c["s"] if fmt != "nv" else torch.empty((M, iq.fp4_scale_bytes(fmt)), dtype=torch.uint8, device=dev)
+            fns.append(step_fn(c, fmt, s=s_f))
+        for f in fns:
+            f()
+        f_ms = flushed_ms(None, lambda i: fns[i % len(fns)](), 50)
+        fp4_formats[fmt] = {"us_per_step": statistics.median(f_ms) * 1e3, "mean_us_per_step": sum(f_ms) / 50 * 1e3,
+                            "tokens_per_s": M / (statistics.median(f_ms) * 1e-3),
                             "scale_bytes_per_token": iq.fp4_scale_bytes(fmt)}
+        del fns
 
     # ------------------------------------------------- the quantizer alone
     xb = W.quant_blocks_input(M_PREFILL, K_QUANT, seed=1)
-    X = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
-    Y = torch.empty((M_PREFILL, K_QUANT), dtype=torch.uint8, device=dev)
-    S = torch.empty(((K_QUANT + 511) // 512, (M_PREFILL + 3) // 4 * 4), dtype=torch.int32, device=dev)
-    for _ in range(3):
-        iq.fp8_quant_1x128_ue8m0(X, y=Y, scales=S)
-    torch.cuda.synchronize()
-    qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for a, b in qev:
-        flush_l2()
-        a.record(stream)
-        iq.fp8_quant_1x128_ue8m0(X, y=Y, scales=S)
-        b.record(stream)
-    torch.cuda.synchronize()
-    q_ms = sum(a.elapsed_time(b) for a, b in qev) / len(qev)
-    q_bytes = M_PREFILL * K_QUANT * 3 + S.numel() * 4
+    X0 = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(dev)
+    q_sets = []
+    q_set_bytes = M_PREFILL * K_QUANT * 3
+    for i in range(sets_for(q_set_bytes)):
+        q_sets.append((X0.clone(), torch.empty((M_PREFILL, K_QUANT), dtype=torch.uint8, device=dev),
+                       torch.empty(((K_QUANT + 511) // 512, (M_PREFILL + 3) // 4 * 4), dtype=torch.int32,
+                                   device=dev)))
+    q_fns = [(lambda t=t: iq.fp8_quant_1x128_ue8m0(t[0], y=t[1], scales=t[2])) for t in q_sets]
+    for f in q_fns:
+        f()
+    qm = flushed_ms(None, lambda i: q_fns[i % len(q_fns)](), args.steps)
+    q_ms = sum(qm) / len(qm)
+    qbb, qbb_total = time_back_to_back(q_fns, args.steps, 2 * len(q_sets))
+    q_bytes = M_PREFILL * K_QUANT * 3 + q_sets[0][2].numel() * 4
     q_gbs = q_bytes / (q_ms * 1e-3) / 1e9
+    q_bb_gbs = q_bytes / (qbb_total / len(qbb) * 1e-3) / 1e9
     quantizer = {"workload": "BF16 [4632, 7168] -> E4M3 + packed UE8M0 scales", "value": q_gbs, "unit": "GB/s",
-                 "avg_launch_ms": q_ms,
+                 "avg_launch_ms": q_ms, "median_launch_ms": statistics.median(qm),
+                 "launches": "each after an L2 flush, events around the launch",
+                 "back_to_back_gbs": q_bb_gbs,
+                 "back_to_back_how": f"launches back to back over {len(q_sets)} buffer sets: each also writes back "
+                                     f"the previous launch's output",
                  "roofline": {"kernel": "quant_1x128_kernel", "bound": "hbm", "achieved": q_gbs, "peak": hbm_peak,
                               "unit": "GB/s", "frac": q_gbs / hbm_peak, "traffic": kernel_traffic("quant_1x128_kernel"),
                               "peak_source": peak_kind, "bytes_per_launch": q_bytes,
-                              "frac_of_nominal_hbm": q_gbs / NOMINAL_HBM_GBS}}
-
+                              "frac_of_nominal_hbm": q_gbs / NOMINAL_HBM_GBS,
+                              "back_to_back_frac": q_bb_gbs / hbm_peak}}
+    del q_sets, q_fns, X0
     # ------------------------------------------- decode under graph replay
     # Decode steps (N(0,1) latent, random positions) captured in a CUDA graph
     # per token count and per route (the small-M swapped-operand kernel, the
@@ -453,7 +513,7 @@ def run_ours(args):
     # (302 MB, more than twice L2), so that every call reads W from HBM.  Also
     # the replay of a graph holding one call (includes the graph launch).
     n_rot = 24
-    w_rot = [w.clone() for _ in range(n_rot)]
+    w_rot = [w0.clone() for _ in range(n_rot)]
 
     def graph_us_per_call(calls, total):
         side = torch.cuda.Stream()
@@ -495,9 +555,9 @@ def run_ours(args):
         for route, threshold in (("small_m", iq.SMALL_M_MAX), ("cta_pair", 0)):
             old = iq.set_small_m_threshold(threshold)
             try:
-                hot = graph_us_per_call([call(w)] * n_rot, 1000)
+                hot = graph_us_per_call([call(w0)] * n_rot, 1000)
                 cold = graph_us_per_call([call(wt) for wt in w_rot], 1000)
-                one = graph_us_per_call([call(w)], 1000)
+                one = graph_us_per_call([call(w0)], 1000)
             finally:
                 iq.set_small_m_threshold(old)
             entry[route] = {"us_per_call_w_in_l2": hot, "us_per_call_w_from_hbm": cold,
@@ -510,57 +570,56 @@ def run_ours(args):
     del w_rot
 
     # ------------------------------------------------------ token sweep
-    # Chain and quantizer-alone at each sweep point (L2 flushed before each
-    # timed launch); inputs generated on the device: N(0,1), 0.5% x100
-    # outliers, random positions.
+    # Chain and quantizer-alone at each sweep point: each timed call after an
+    # L2 flush, and (extra keys) back to back over rotating buffer sets whose
+    # total is over twice L2; inputs generated on the device: N(0,1), 0.5% x100
+    # outliers, random positions.  W is rotated with the sets.
     sweep = {}
     gen = torch.Generator(device=dev)
     gen.manual_seed(4)
+
+    def bf16_input(rows, cols):
+        t = torch.randn((rows, cols), generator=gen, device=dev)
+        hit = torch.rand((rows, cols), generator=gen, device=dev) < 0.005
+        return torch.where(hit, t * 100.0, t).to(torch.bfloat16)
+
     for Ms in (128, 512, 1024, 4632, 16384, 65536):
-        def bf16_input(rows, cols):
-            t = torch.randn((rows, cols), generator=gen, device=dev)
-            hit = torch.rand((rows, cols), generator=gen, device=dev) < 0.005
-            return torch.where(hit, t * 100.0, t).to(torch.bfloat16)
         lat_s = bf16_input(Ms, K_LATENT)
         pos_s = torch.randint(0, 163840, (Ms,), generator=gen, device=dev, dtype=torch.int32)
-        q_s = torch.empty((Ms, N_Q // 2), dtype=torch.uint8, device=dev)
-        s_s = torch.empty((Ms, N_Q // 32), dtype=torch.uint8, device=dev)
-        work_s = torch.empty(iq.prepare_q_workspace_bytes(Ms), dtype=torch.uint8, device=dev)
-        reps = 10 if Ms >= 16384 else 20
-        for _ in range(3):
-            iq.prepare_q(lat_s, w, ws, pos_s, q_fp4=q_s, q_sf=s_s, workspace=work_s)
-        chain_t = []
-        for _ in range(reps):
-            flush_l2()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            iq.prepare_q(lat_s, w, ws, pos_s, q_fp4=q_s, q_sf=s_s, workspace=work_s)
-            b.record()
-            chain_t.append((a, b))
-        torch.cuda.synchronize()
-        c_ms = sum(a.elapsed_time(b) for a, b in chain_t) / reps
-        del lat_s, q_s, s_s, work_s
+        per_set = Ms * (2 * K_LATENT + 4 + N_Q // 2 + N_Q // 32) + iq.prepare_q_workspace_bytes(Ms) + w0.numel()
+        sets = []
+        for i in range(sets_for(per_set)):
+            sets.append({"lat": lat_s.clone(), "w": w0.clone(), "p": pos_s.clone(),
+                         "q": torch.empty((Ms, N_Q // 2), dtype=torch.uint8, device=dev),
+                         "s": torch.empty((Ms, N_Q // 32), dtype=torch.uint8, device=dev),
+                         "work": torch.empty(iq.prepare_q_workspace_bytes(Ms), dtype=torch.uint8, device=dev)})
+        fns = [step_fn(c) for c in sets]
+        reps = 20 if Ms >= 16384 else 50
+        for f in fns:
+            f()
+        c_ms = flushed_ms(None, lambda i: fns[i % len(fns)](), reps)
+        cbb, cbb_total = time_back_to_back(fns, reps, 2 * len(sets))
+        del sets, fns, lat_s
         xq_in = bf16_input(Ms, K_QUANT)
-        yq = torch.empty((Ms, K_QUANT), dtype=torch.uint8, device=dev)
-        sq = torch.empty(((K_QUANT + 511) // 512, (Ms + 3) // 4 * 4), dtype=torch.int32, device=dev)
-        for _ in range(3):
-            iq.fp8_quant_1x128_ue8m0(xq_in, y=yq, scales=sq)
-        qt = []
-        for _ in range(reps):
-            flush_l2()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            iq.fp8_quant_1x128_ue8m0(xq_in, y=yq, scales=sq)
-            b.record()
-            qt.append((a, b))
-        torch.cuda.synchronize()
-        qs_ms = sum(a.elapsed_time(b) for a, b in qt) / reps
-        qbytes = Ms * K_QUANT * 3 + sq.numel() * 4
-        del xq_in, yq, sq
+        qsets = []
+        for i in range(sets_for(Ms * K_QUANT * 3)):
+            qsets.append((xq_in.clone() if i else xq_in, torch.empty((Ms, K_QUANT), dtype=torch.uint8, device=dev),
+                          torch.empty(((K_QUANT + 511) // 512, (Ms + 3) // 4 * 4), dtype=torch.int32, device=dev)))
+        qfns = [(lambda t=t: iq.fp8_quant_1x128_ue8m0(t[0], y=t[1], scales=t[2])) for t in qsets]
+        for f in qfns:
+            f()
+        qm = flushed_ms(None, lambda i: qfns[i % len(qfns)](), reps)
+        qs_ms = sum(qm) / reps
+        qbb, qbb_total = time_back_to_back(qfns, reps, 2 * len(qsets))
+        qbytes = Ms * K_QUANT * 3 + qsets[0][2].numel() * 4
+        del qsets, qfns, xq_in
         flops = Ms * FLOPS_PER_TOKEN
+        cm = statistics.median(c_ms)
         sweep[str(Ms)] = {
-            "chain_us": c_ms * 1e3, "tokens_per_s": Ms / (c_ms * 1e-3),
-            "chain_tflops": flops / (c_ms * 1e-3) / 1e12, "chain_frac_of_fp8_peak": flops / (c_ms * 1e-3) / 1e12 / fp8_peak_tflops,
+            "chain_us": cm * 1e3, "chain_mean_us": sum(c_ms) / reps * 1e3, "tokens_per_s": Ms / (cm * 1e-3),
+            "chain_back_to_back_us": cbb_total / reps * 1e3,
+            "quant7168_back_to_back_gbs": qbytes / (qbb_total / reps * 1e-3) / 1e9,
+            "chain_tflops": flops / (cm * 1e-3) / 1e12, "chain_frac_of_fp8_peak": flops / (cm * 1e-3) / 1e12 / fp8_peak_tflops,
             "quant7168_us": qs_ms * 1e3, "quant7168_gbs": qbytes / (qs_ms * 1e-3) / 1e9,
             "quant7168_frac_of_hbm": qbytes / (qs_ms * 1e-3) / 1e9 / hbm_peak}
     # The quantizer's fraction also against the best rate any of its launches
@@ -568,7 +627,6 @@ def run_ours(args):
     best_q = max([q_gbs] + [v["quant7168_gbs"] for v in sweep.values()])
     quantizer["roofline"]["best_kernel_gbs_in_run"] = best_q
     quantizer["roofline"]["frac_of_best_in_run"] = q_gbs / best_q
-
     # ------------------------------------------ end to end through the C ABI
     # iq_prepare_q_host on page-locked host buffers: every step reads the
     # latent rows and positions from host memory and returns the FP4 codes and
@@ -580,7 +638,7 @@ def run_ours(args):
     work_h = torch.empty(iq.prepare_q_host_workspace_bytes(M), dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        iq.prepare_q_host(h_lat, w, ws, h_pos, q_fp4=h_q, q_sf=h_s, workspace=work_h, stream=stream)
+        iq.prepare_q_host(h_lat, w0, ws, h_pos, q_fp4=h_q, q_sf=h_s, workspace=work_h, stream=stream)
 
     for _ in range(3):
         e2e_step()
@@ -617,11 +675,13 @@ def run_ours(args):
                                    "RoPE (positions 0..4631) -> Hadamard-128 -> MXFP4 [4632, 4096] + UE8M0 "
                                    "[4632, 256]",
                        "M": M, "K": K_LATENT, "N": N_Q, "parallelism": f"replicas x{world}",
-                       "l2": "flushed between timed steps (256 MB write then 256 MB read), outside the event intervals"},
+                       "l2": "flushed between timed steps (256 MB write then 256 MB read), outside the event "
+                             "intervals; back_to_back: rotating buffer sets over twice the L2 size"},
             "roofline": roofline, "quantizer": quantizer, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": 2 * args.steps,
             "clocks": clocks.summary(),
             "k1_chain_avg_ms": k1_avg_ms, "wall_s_timed": t_wall, "step_stats": step_stats,
+            "back_to_back": back_to_back,
             "decode": decode, "sweep": sweep, "fp4_formats": fp4_formats,
         }
         print(json.dumps(line), flush=True)

@@ -36,24 +36,20 @@ std::atomic<int> g_small_m_max{iq::kSmallMMax};
 std::atomic<int> g_tile_n_override{0};   // 0: by token count; else 128 or 256
 std::atomic<int> g_order_override{0};    // 0: by token count; 1 feature-major; 2 token-major
 
-// Tile width and order of the CTA-pair kernel for M tokens.  One head per
-// tile up to 1024 tokens: the two-head tile leaves SMs idle there (at most
-// 4 x 32 tiles for 76 pairs) and its single accumulator serializes each
-// tile's epilogue with the next tile's MMAs.  Token-major order from 16384
-// tokens, where X and the outputs no longer fit in L2.
-constexpr int kNarrowTileMaxTokens = 1024;
-constexpr int kTokenMajorMinTokens = 16384;
-
-int gemm_tile_n(int M) {
+// Tile width and order of the CTA-pair kernel.  Measured on GB300 (kernel
+// alone, L2 flushed, 65 ... 65536 tokens): the two-head tile is as fast as
+// the one-head tile up to 256 tokens and faster from 512 (up to 1.7x at
+// large M, where the one-head tile moves half again as many operand bytes
+// from L2 per FLOP); token-major order is as fast or faster at every size,
+// by 4 % at 4632 tokens and 16 % at 65536.
+int gemm_tile_n(int) {
   const int o = g_tile_n_override.load(std::memory_order_relaxed);
-  if (o == 128 || o == 256) return o;
-  return M <= kNarrowTileMaxTokens ? 128 : 256;
+  return o == 128 ? 128 : 256;
 }
 
-int gemm_token_major(int M) {
+int gemm_token_major(int) {
   const int o = g_order_override.load(std::memory_order_relaxed);
-  if (o == 1 || o == 2) return o == 2 ? 1 : 0;
-  return M >= kTokenMajorMinTokens ? 1 : 0;
+  return o == 1 ? 0 : 1;
 }
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 
@@ -244,6 +240,18 @@ iq_status iq_device_status(uint32_t* flags, int reset) {
 void iq_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs); }
 
 void iq_debug_fail_next_setups(int count) { g_fail_setups.store(count > 0 ? count : 0); }
+
+iq_status iq_debug_e2m1_codes(const float* x, long long n, uint8_t* codes, cudaStream_t stream) {
+  if (n < 0) return IQ_ERR_ARG;
+  if (n % 8 != 0) return IQ_ERR_SHAPE;
+  if (n == 0) return IQ_OK;
+  if (!x || !codes) return IQ_ERR_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 8)) return IQ_ERR_ALIGN;
+  int max_pairs = 0;
+  const iq_status st = device_setup(&max_pairs);
+  if (st != IQ_OK) return st;
+  return iq::launch_e2m1_codes(x, n, codes, stream) == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
+}
 
 size_t iq_selftest_workspace(void) {
   // x_sf [3][256] words, positions [256], w_sf [64][12] bytes, q_sf [256][256]

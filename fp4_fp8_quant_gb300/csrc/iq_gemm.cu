@@ -77,8 +77,12 @@ constexpr int kNumEpiWarps = 8;
 constexpr int kThreads = (2 + kNumEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;                  // accumulators: columns 0..255
-constexpr uint32_t kSfaCol = 256;                // + 8 g, 4 columns each
-constexpr uint32_t kSfbCol = 288;                // + 8 g, 4 columns per head of the tile
+// Scale factors in tensor memory, two buffers (tile parity) so that a tile's
+// copies are issued before the accumulator hand-off from the previous tile:
+// SFA at kSfaCol + 32 b + 8 g (4 columns), SFB at kSfbCol + 32 b + 8 g + 4 h.
+constexpr uint32_t kSfaCol = 256;
+constexpr uint32_t kSfbCol = 320;
+constexpr uint32_t kSfBufCols = 32;
 constexpr int kSfaWords = kScaleGroups * 128;    // per buffer
 constexpr int kOutHeadBytes = BM * 64;           // FP4 codes of one head of the CTA's rows
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1;
@@ -109,6 +113,7 @@ struct K2Layout {
   static_assert(kOffB % 1024 == 0 && kBBytes % 1024 == 0 && kOffOut % 1024 == 0, "swizzled tiles");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kAccBufs * kBN <= static_cast<int>(kSfaCol), "accumulators below the scale columns");
+  static_assert(kSfbCol + 2 * kSfBufCols <= kTmemCols && kSfaCol + 2 * kSfBufCols <= kSfbCol, "scale columns");
 };
 
 __device__ __forceinline__ void fail(volatile uint32_t* abort_flag, uint32_t bit) {
@@ -329,10 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  // Launched with programmatic stream serialization: everything above
-  // overlapped the preceding kernel; nothing below runs before it completed
-  // (no global memory is read or written before this point).
-  grid_dependency_wait();
 
   // Leader-CTA addresses of the barriers that collect the pair's work.
   const uint32_t full_leader0 = mapa_shared(smem_u32(&full[0]), 0);
@@ -342,12 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Pair tile pt covers token rows [256 mp, +256) (split by CTA rank) and
   // features [kBN n, +kBN).  Each pair takes a contiguous run of tiles.  In
   // feature-major order (mp = pt % num_m_pairs) consecutive tiles share their
-  // heads: W stays hot in L2 and the weight scales are staged and copied
-  // into tensor memory only when the heads change.  In token-major order
-  // (mp = pt / n_tiles) consecutive tiles share their token rows, so the pairs
-  // running at one time read few distinct X row blocks, each from HBM once,
-  // while W (12.6 MB) stays in L2: the order for token counts whose X and
-  // outputs do not fit in L2.
+  // heads.  In token-major order (mp = pt / n_tiles, the default) consecutive
+  // tiles share their token rows, so the pairs running at one time read few
+  // distinct X row blocks, each from HBM once, while W (12.6 MB) stays in L2;
+  // measured as fast or faster at every token count.
   constexpr int n_tiles = kQDim / kBN;
   const int num_pairs = static_cast<int>(cluster_count_x());
   const int tiles_per_pair = (args.num_pair_tiles + num_pairs - 1) / num_pairs;
@@ -358,21 +357,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tile_mp = [&](int pt) { return token_major ? pt / n_tiles : pt % num_m_pairs; };
   auto tile_n = [&](int pt) { return token_major ? pt % n_tiles : pt / num_m_pairs; };
   auto tile_m0 = [&](int pt) { return (tile_mp(pt) * kPair + static_cast<int>(rank)) * BM; };
-  auto new_heads = [&](int pt) { return pt == first_pt || tile_n(pt - 1) != tile_n(pt); };
+
+  // The producer's first tile: W and its scales are inputs the preceding
+  // kernel does not write (the quantizer writes only the FP8 latent and its
+  // scales), so the first pass of W loads over the ring and the first
+  // weight-scale words are issued before the dependency wait and overlap
+  // that kernel.  The stages are fresh, so no release wait precedes them; the
+  // leader's expected byte count covers the X loads issued after the wait.
+  uint32_t rb[kScaleGroups][L::kHeads];   // producer: the tile's heads' weight-scale words per group
+  auto fetch_w_scales = [&](int pt) {
+    if (pt >= end_pt) return;
+    const int n_tile = tile_n(pt);
+#pragma unroll
+    for (int g = 0; g < kScaleGroups; ++g) {
+#pragma unroll
+      for (int h = 0; h < L::kHeads; ++h) {
+        const uint8_t* ws = args.w_sf + (n_tile * L::kHeads + h) * kNumKBlocks + 4 * g;
+        rb[g][h] = static_cast<uint32_t>(__ldg(ws)) | (static_cast<uint32_t>(__ldg(ws + 1)) << 8) |
+                   (static_cast<uint32_t>(__ldg(ws + 2)) << 16) | (static_cast<uint32_t>(__ldg(ws + 3)) << 24);
+      }
+    }
+  };
+  const bool have_tile = first_pt < end_pt;
+  if (warp == 0) {
+    if constexpr (!kNoLoads) {
+      if (lane == 0 && have_tile) {
+        const int n0 = tile_n(first_pt) * kBN + static_cast<int>(rank) * (kBN / kPair);
+        for (int kb = 0; kb < kStages; ++kb) {
+          if (leader) mbar_arrive_expect_tx(&full[kb], L::kStageTx);
+          tma_load_2d_pair(sB + kb * L::kBBytes, &tm_w, full_leader0 + 8u * kb, kb * BK, n0);
+        }
+      }
+    }
+    fetch_w_scales(first_pt);
+  }
+  // Launched with programmatic stream serialization: everything above
+  // overlapped the preceding kernel; nothing below runs before it completed
+  // (apart from the W loads and weight-scale reads above, no global memory is
+  // read or written before this point).
+  grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, issued_phase = 0;   // per stage: a load was issued / its phase
+    // The first tile's X loads of the first pass go out at once (their W
+    // halves are already in flight), ahead of the scale-word reads.
+    if constexpr (!kNoLoads) {
+      if (lane == 0 && have_tile) {
+        const int m0 = tile_m0(first_pt);
+        for (int kb = 0; kb < kStages; ++kb)
+          tma_load_2d_pair(sA + kb * kABytes, &tm_x, full_leader0 + 8u * kb, kb * BK, m0);
+        issued_mask = (1u << kStages) - 1u;
+        issued_phase = 0u;
+        phase = 1;
+      }
+    }
     // The next tile's scale words are fetched into registers while the
     // current tile's K-blocks stream, so no global-load latency sits at a
     // tile boundary.  ra: this lane's 4 rows x 3 groups of activation-scale
-    // words; rb: the tile's heads' weight-scale words per group.
-    uint32_t ra[kScaleGroups][4], rb[kScaleGroups][L::kHeads];
-    auto fetch_scales = [&](int pt) {
+    // words (written by the preceding kernel: read after the wait).
+    uint32_t ra[kScaleGroups][4];
+    auto fetch_x_scales = [&](int pt) {
       if (pt >= end_pt) return;
       const int m0 = tile_m0(pt);
-      const int n_tile = tile_n(pt);
 #pragma unroll
       for (int g = 0; g < kScaleGroups; ++g) {
 #pragma unroll
@@ -380,17 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = m0 + c * 32 + lane;
           ra[g][c] = m < args.m_al ? ld_dependent_u32(args.x_sf + static_cast<long long>(g) * args.m_al + m) : 0u;
         }
-        if (new_heads(pt)) {
-#pragma unroll
-          for (int h = 0; h < L::kHeads; ++h) {
-            const uint8_t* ws = args.w_sf + (n_tile * L::kHeads + h) * kNumKBlocks + 4 * g;
-            rb[g][h] = static_cast<uint32_t>(__ldg(ws)) | (static_cast<uint32_t>(__ldg(ws + 1)) << 8) |
-                       (static_cast<uint32_t>(__ldg(ws + 2)) << 16) | (static_cast<uint32_t>(__ldg(ws + 3)) << 24);
-          }
-        }
       }
     };
-    fetch_scales(first_pt);
+    fetch_x_scales(first_pt);
     int local = 0;
     for (int pt = first_pt; pt < end_pt; ++pt, ++local) {
       // Every exit decision is made warp-uniform: the lanes must stay
@@ -405,29 +445,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Scale factors in the tcgen05.cp 32x128b layout: word [r * 4 + c] of a
       // 128-row tile holds row c * 32 + r.  SFA: this CTA's 128 token rows;
-      // SFB: the tile's heads (128 rows each, all of them in both CTAs),
-      // staged only when the heads differ from the previous tile's (the MMA
-      // issuer copies it only then).
+      // SFB: the tile's heads (128 rows each, all of them in both CTAs).
       uint32_t* sfa = sSfa + buf * kSfaWords;
       uint32_t* sfb = sSfb + buf * L::kSfbWords;
-      const bool stage_sfb = new_heads(pt);
 #pragma unroll
       for (int g = 0; g < kScaleGroups; ++g) {
         *reinterpret_cast<uint4*>(sfa + g * 128 + lane * 4) = make_uint4(ra[g][0], ra[g][1], ra[g][2], ra[g][3]);
-        if (stage_sfb) {
 #pragma unroll
-          for (int h = 0; h < L::kHeads; ++h)
-            *reinterpret_cast<uint4*>(sfb + g * kBN + h * 128 + lane * 4) =
-                make_uint4(rb[g][h], rb[g][h], rb[g][h], rb[g][h]);
-        }
+        for (int h = 0; h < L::kHeads; ++h)
+          *reinterpret_cast<uint4*>(sfb + g * kBN + h * 128 + lane * 4) =
+              make_uint4(rb[g][h], rb[g][h], rb[g][h], rb[g][h]);
       }
       fence_proxy_async_smem();
       __syncwarp();
-      fetch_scales(pt + 1);
+      fetch_x_scales(pt + 1);
+      fetch_w_scales(pt + 1);
       bool ok = true;
       if (lane == 0) {
         mbar_arrive_cluster(sf_full_leader0 + 8u * static_cast<uint32_t>(buf));
-        for (int kb = 0; kb < kNumKBlocks; ++kb) {
+        for (int kb = (local == 0 && !kNoLoads) ? kStages : 0; kb < kNumKBlocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, timeout)) {
             fail(abort_flag, kStatusProducerWait);
             ok = false;
@@ -476,26 +512,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (*abort_flag) break;
           const int buf = local & 1;
           const int acc = local % L::kAccBufs;
-          if (!mbar_wait(&sf_full[buf], (local >> 1) & 1, timeout) ||
-              !mbar_wait(&tmem_empty[acc], ((local / L::kAccBufs) & 1) ^ 1, timeout)) {
+          // The scale factors of this tile go to TMEM buffer `buf`, last read by
+          // the tile two before, which is complete once that tile's
+          // accumulator was drained: with one accumulator that was waited for
+          // at the previous tile, so the copies are issued before this tile's
+          // accumulator wait (off the hand-off); with two, after it.
+          const uint32_t sfa_col = kSfaCol + kSfBufCols * static_cast<uint32_t>(buf);
+          const uint32_t sfb_col = kSfbCol + kSfBufCols * static_cast<uint32_t>(buf);
+          auto copy_scales = [&]() {
+            tc_fence_after_sync();
+            const uint32_t* sfa = sSfa + buf * kSfaWords;
+            const uint32_t* sfb = sSfb + buf * L::kSfbWords;
+#pragma unroll
+            for (int g = 0; g < kScaleGroups; ++g) {
+              tc_cp_32x128b_warpx4_pair(tmem + sfa_col + 8 * g, smem_desc_sf(smem_u32(sfa + g * 128)));
+#pragma unroll
+              for (int h = 0; h < L::kHeads; ++h)
+                tc_cp_32x128b_warpx4_pair(tmem + sfb_col + 8 * g + 4 * h,
+                                          smem_desc_sf(smem_u32(sfb + g * kBN + h * 128)));
+            }
+            tc_commit_pair(&sf_empty[buf], kPairMask);
+          };
+          if (!mbar_wait(&sf_full[buf], (local >> 1) & 1, timeout)) {
+            fail(abort_flag, kStatusMmaWait);
+            break;
+          }
+          if constexpr (L::kAccBufs == 1) copy_scales();
+          if (!mbar_wait(&tmem_empty[acc], ((local / L::kAccBufs) & 1) ^ 1, timeout)) {
             fail(abort_flag, kStatusMmaWait);
             break;
           }
           tc_fence_after_sync();
-          const uint32_t* sfa = sSfa + buf * kSfaWords;
-          const uint32_t* sfb = sSfb + buf * L::kSfbWords;
-          const bool copy_sfb = new_heads(pt);
-#pragma unroll
-          for (int g = 0; g < kScaleGroups; ++g) {
-            tc_cp_32x128b_warpx4_pair(tmem + kSfaCol + 8 * g, smem_desc_sf(smem_u32(sfa + g * 128)));
-            if (copy_sfb) {
-#pragma unroll
-              for (int h = 0; h < L::kHeads; ++h)
-                tc_cp_32x128b_warpx4_pair(tmem + kSfbCol + 8 * g + 4 * h,
-                                          smem_desc_sf(smem_u32(sfb + g * kBN + h * 128)));
-            }
-          }
-          tc_commit_pair(&sf_empty[buf], kPairMask);
+          if constexpr (L::kAccBufs == 2) copy_scales();
           const uint32_t d_tmem = tmem + kAccCol + static_cast<uint32_t>(acc * kBN);
           // The K loop does little between MMAs: a tile is exactly two
           // passes over the ring, so every stage index, barrier phase, scale
@@ -519,8 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < BK / 32; ++k) {
               // advance 32 bytes along K inside the 128-byte swizzle atom
-              tc_mma_mxf8_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, tmem + kSfaCol + sf_off,
-                               tmem + kSfbCol + sf_off, (kb | k) != 0);
+              tc_mma_mxf8_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, tmem + sfa_col + sf_off,
+                               tmem + sfb_col + sf_off, (kb | k) != 0);
             }
             tc_commit_pair(&empty[s], kPairMask);   // frees the stage in both CTAs
           }
@@ -596,7 +644,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_store_commit();
       }
     }
-    if (store_issuer) tma_store_wait_all();
+    // The staging tile must stay valid until the last bulk stores have read
+    // it; their writes to global memory complete with the grid.
+    if (store_issuer) tma_store_wait_read();
   }
 
   // Neither CTA leaves (or frees tensor memory) while the pair may still use

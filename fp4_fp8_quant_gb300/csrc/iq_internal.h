@@ -79,6 +79,9 @@ cudaError_t launch_quant_1x128_host_rows(const void* x, int M, int K, long long 
                                          int32_t* sf, const int32_t* pos_src, int32_t* pos_dst, int max_blocks,
                                          cudaStream_t stream);
 
+// The FP4 stage's float -> E2M1 conversion alone, one code per byte; n % 8 == 0.
+cudaError_t launch_e2m1_codes(const float* x, long long n, uint8_t* codes, cudaStream_t stream);
+
 // Kernel attribute set-up of the fused GEMM on the current device; returns
 // how many of its CTA pairs fit on the device at once.
 cudaError_t gemm_setup_device(int* max_pairs);

@@ -180,7 +180,29 @@ __global__ void __launch_bounds__(kHostThreads)
 }
 
 
+// The FP4 stage's element conversion alone (the one both fused GEMM kernels
+// use): eight floats per thread through cvt_e2m1x8, one code per output byte.
+__global__ void e2m1_codes_kernel(const float* __restrict__ x, long long n8, uint8_t* __restrict__ out) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(x)[2 * i];
+  const float4 b = reinterpret_cast<const float4*>(x)[2 * i + 1];
+  const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const uint32_t c = cvt_e2m1x8(v);
+  uint2 o;
+  o.x = (c & 0xFu) | ((c >> 4) & 0xFu) << 8 | ((c >> 8) & 0xFu) << 16 | ((c >> 12) & 0xFu) << 24;
+  o.y = ((c >> 16) & 0xFu) | ((c >> 20) & 0xFu) << 8 | ((c >> 24) & 0xFu) << 16 | ((c >> 28) & 0xFu) << 24;
+  reinterpret_cast<uint2*>(out)[i] = o;
+}
+
 }  // namespace
+
+cudaError_t launch_e2m1_codes(const float* x, long long n, uint8_t* codes, cudaStream_t stream) {
+  const long long n8 = n / 8;
+  const long long blocks = (n8 + 255) / 256;
+  e2m1_codes_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, n8, codes);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant_1x128(const void* x, int M, int K, long long ldx, void* y, long long ldy, int32_t* sf,
                                cudaStream_t stream) {

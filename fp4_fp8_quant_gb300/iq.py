@@ -34,6 +34,7 @@ SIGNATURES = {
     "iq_selftest_workspace": (_SZ, []),
     "iq_selftest_wait_timeout": (_I, [_P, _SZ, ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint32), _P]),
     "iq_debug_fail_next_setups": (None, [_I]),
+    "iq_debug_e2m1_codes": (_I, [_P, ctypes.c_longlong, _P, _P]),
     "iq_fp8_scale_words": (_SZ, [_I, _I]),
     "iq_fp8_quant_1x128_ue8m0": (_I, [_P, _I, _I, _I, _P, _I, _P, _P]),
     "iq_prepare_q_workspace": (_SZ, [_I]),

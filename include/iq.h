@@ -103,6 +103,13 @@ iq_status iq_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t ti
  * failed set-up is not cached: the next call on the device tries again. */
 void iq_debug_fail_next_setups(int count);
 
+/* The FP4 stage's element conversion alone, for testing it directly:
+ * codes[i] (low nibble) = E2M1 code of x[i], round to nearest even,
+ * saturating at +-6, sign of zero kept -- the conversion both fused GEMM
+ * kernels apply to z * 2^-e.  x: n float32, 16-byte aligned; codes: n bytes,
+ * 8-byte aligned; n % 8 == 0 (else IQ_ERR_SHAPE).  One kernel launch. */
+iq_status iq_debug_e2m1_codes(const float* x, long long n, uint8_t* codes, cudaStream_t stream);
+
 /* Token-count route of the fused GEMM (operation 2).  Calls with
  * 1 <= M <= threshold run the small-M kernel, which swaps the MMA operands
  * (the weights on the MMA's M side, the tokens on its N side), the variant the
@@ -120,11 +127,12 @@ int iq_set_small_m_threshold(int max_tokens);
 int iq_small_m_threshold(void);
 
 /* Tuning override of the CTA-pair kernel's tiling, for measurements.  By
- * default the kernel takes one head (128 output features) per pair tile for
- * M <= 1024 and two heads (256) above, and orders the pair tiles
- * feature-major below 16384 tokens and token-major from there.  tile_n: 128
- * or 256 forces that width, any other value restores the default; order: 1
- * forces feature-major, 2 token-major, any other value restores the default.
+ * default the kernel takes two heads (256 output features) per pair tile and
+ * orders the pair tiles token-major (consecutive tiles of a CTA pair share
+ * their 256 token rows).  tile_n: 128 (one head per tile, two accumulators
+ * in tensor memory) or 256 forces that width, any other value restores the
+ * default; order: 1 forces feature-major (consecutive tiles share their
+ * heads), 2 token-major, any other value restores the default.
  * Results are the same under every setting (the same sums in the same order
  * per output).  Process-wide; applies to later calls. */
 void iq_set_gemm_tiling(int tile_n, int order);

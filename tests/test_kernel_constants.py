@@ -13,6 +13,7 @@ from decimal import Decimal, getcontext
 from pathlib import Path
 
 import numpy as np
+import pytest
 
 from oracle import iq_oracle as O
 
@@ -85,3 +86,33 @@ def test_replay_catches_a_wrong_constant():
     bad[3] += 1
     vals = O.e4m3_value_table()
     assert any(_replay(c, sub, bad) != np.float32(1) / np.float32(vals[c]) for c in range(1, 0x7F))
+
+
+@pytest.mark.gpu
+def test_gpu_e2m1_conversion_dense_sweep(cuda_device):
+    """The GPU's float -> E2M1 conversion (the one both fused GEMM kernels
+    use) on a dense float32 sweep of [-7, 7] with every rounding midpoint, the
+    float32 neighbours of each midpoint and grid value, signed zeros and
+    values past the saturation bound, against the oracle's round-to-nearest-
+    even rule."""
+    import torch
+    from fp4_fp8_quant_gb300 import iq
+    from oracle import iq_oracle as O
+    grid = O.e2m1_value_table()[:8].astype(np.float32)
+    mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)
+    special = np.concatenate([mids, grid, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(10)),
+                              np.nextafter(grid, np.float32(0)), np.nextafter(grid, np.float32(10)),
+                              [6.5, 7.0, 1e30, 0.0, 1e-30, 1e-45]]).astype(np.float32)
+    dense = np.linspace(-7, 7, 1 << 21, dtype=np.float32)
+    x = np.concatenate([dense, special, -special]).astype(np.float32)
+    x = np.concatenate([x, np.zeros((-len(x)) % 8, np.float32)])
+    x[-1] = np.float32(-0.0)
+    xd = torch.from_numpy(x).cuda()
+    codes = torch.empty(len(x), dtype=torch.uint8, device="cuda")
+    rc = iq.lib().iq_debug_e2m1_codes(xd.data_ptr(), len(x), codes.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    got = codes.cpu().numpy()
+    want = O.round_to_e2m1_codes(x.astype(np.float64))      # saturates at 6, keeps the sign
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, first x={x[bad[:5]]} got={got[bad[:5]]} want={want[bad[:5]]}"
