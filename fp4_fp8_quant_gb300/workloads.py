@@ -159,3 +159,36 @@ def sweep_chain(M: int, seed: int = 4):
 def decode_chain(M: int, seed: int = 2):
     """Decode batch of M tokens: plain N(0,1) latent, random positions."""
     return chain_workload(M, seed, 0.0, 1.0)
+
+
+# Inputs of the downstream indexer consumer (logits and top-k).
+_FP4_MAGNITUDE_P = np.array([0.22, 0.2, 0.16, 0.14, 0.1, 0.08, 0.06, 0.04])   # codes 0..7
+
+
+def mxfp4_codes(rows: int, dims: int, rng: np.random.Generator) -> np.ndarray:
+    """Packed E2M1 codes [rows, dims / 2] (element 2i in the low nibble):
+    magnitude codes drawn from a fixed distribution favouring small values,
+    random signs.  A draw of codes, not a quantization of anything."""
+    mag = rng.choice(8, size=(rows, dims), p=_FP4_MAGNITUDE_P).astype(np.uint8)
+    sign = (rng.random((rows, dims)) < 0.5).astype(np.uint8) << 3
+    c = mag | sign
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+def indexer_inputs(M: int, N: int, seed: int = 0, causal: bool = True):
+    """Query side [M, 4096] codes + [M, 256] UE8M0 scale bytes (the layout
+    iq_prepare_q writes), key cache [N, 64] codes + [N, 4] scale bytes, per-head
+    weights float32 [M, 64] N(0, 1/64), and visible lengths int32 [M]: the M
+    queries are the last M positions of an N-token sequence (L = position + 1)
+    when causal, else every key is visible."""
+    rng = _rng(3000 + seed)
+    q = mxfp4_codes(M * N_HEADS, HEAD_DIM, rng).reshape(M, Q_DIM // 2)
+    q_sf = rng.integers(122, 127, size=(M, Q_DIM // 32)).astype(np.uint8)
+    k = mxfp4_codes(N, HEAD_DIM, rng)
+    k_sf = rng.integers(122, 127, size=(N, HEAD_DIM // 32)).astype(np.uint8)
+    w = (rng.standard_normal((M, N_HEADS)) / 8).astype(np.float32)
+    if causal:
+        lengths = np.clip(np.arange(N - M, N) + 1, 0, N).astype(np.int32)
+    else:
+        lengths = np.full(M, N, np.int32)
+    return q, q_sf, k, k_sf, w, lengths

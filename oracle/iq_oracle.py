@@ -372,3 +372,79 @@ def prequant_q_rows(latent_bits: np.ndarray, wq: np.ndarray, w_sb: np.ndarray,
     of large problems."""
     rows = np.asarray(rows)
     return prepare_q(latent_bits[rows], wq, w_sb, pos[rows], fmt)
+
+
+# ------------------------------------------- downstream: indexer logits, top-k
+# The consumer of the prepared Q: the sparse-attention indexer's score of
+# every (query token, cached key) pair and the selection of the top-k keys per
+# query ([TS] Summary and Prefill host-sync cleanup: the indexer top-k written
+# straight to its destination).  The pages name this consumer but not its
+# formulas or layouts; the readings (A17-A22 in the design notes):
+#   A17  score I[t, s] = sum_h w[t, h] * max(0, q(t, h) . k(s)) over the 64
+#        heads, q(t, h) the decoded head h of token t's FP4 Q, k(s) the decoded
+#        128-dim key of token s (one key per token, shared by all heads);
+#   A18  the key cache is MXFP4 like Q: codes [N, 64] bytes (element 2i in the
+#        low nibble of byte i), UE8M0 scale bytes [N, 4] (one per 32 dims);
+#   A19  w: float32 [M, 64], given;
+#   A20  query t sees keys s < L[t] (L: int32 [M]); the others score -inf;
+#   A21  top-k: the k visible keys with the largest scores, ties to the
+#        smaller key index, written as int32 indices in ascending order and
+#        padded with -1 when fewer than k keys are visible;
+#   A22  the decision precision: the oracle scores in float64 from the decoded
+#        values (each head's dot product is exact there).
+
+INDEXER_HEADS = 64
+
+
+def decode_mxfp4(codes_packed: np.ndarray, scale_bytes: np.ndarray, block: int = FP4_BLOCK) -> np.ndarray:
+    """Packed E2M1 codes [R, D/2] (element 2i in the low nibble of byte i,
+    A10/A18) and UE8M0 scale bytes [R, D/block] -> float64 [R, D]."""
+    c = np.asarray(codes_packed, dtype=np.uint8)
+    R = c.shape[0]
+    codes = np.empty((R, c.shape[1] * 2), dtype=np.uint8)
+    codes[:, 0::2] = c & 0xF
+    codes[:, 1::2] = c >> 4
+    v = decode_e2m1(codes).reshape(R, -1, block)
+    return (v * decode_ue8m0(scale_bytes)[..., None]).reshape(R, -1)
+
+
+def indexer_logits(q_fp4: np.ndarray, q_sf: np.ndarray, k_fp4: np.ndarray, k_sf: np.ndarray,
+                   weights: np.ndarray, lengths: np.ndarray) -> np.ndarray:
+    """I[t, s] = sum_h w[t, h] max(0, q(t, h) . k(s)) for s < L[t], -inf
+    otherwise (A17-A20).  q_fp4 [M, 4096] / q_sf [M, 256] as iq_prepare_q
+    writes them, k_fp4 [N, 64] / k_sf [N, 4], weights [M, 64], lengths [M].
+    Returns float64 [M, N]."""
+    M = q_fp4.shape[0]
+    N = k_fp4.shape[0]
+    Q = decode_mxfp4(q_fp4.reshape(M * INDEXER_HEADS, HEAD_DIM // 2),
+                     q_sf.reshape(M * INDEXER_HEADS, HEAD_DIM // FP4_BLOCK)).reshape(M, INDEXER_HEADS, HEAD_DIM)
+    K = decode_mxfp4(k_fp4, k_sf)                                   # [N, 128]
+    dots = np.einsum("mhd,nd->mhn", Q, K)                           # exact per head (dyadic values)
+    scores = np.einsum("mh,mhn->mn", np.asarray(weights, np.float64), np.maximum(dots, 0.0))
+    visible = np.arange(N)[None, :] < np.asarray(lengths, np.int64)[:, None]
+    return np.where(visible, scores, -np.inf)
+
+
+def indexer_logit_magnitude(q_fp4, q_sf, k_fp4, k_sf, weights) -> np.ndarray:
+    """S[t, s] = sum_h |w[t, h]| sum_d |q(t, h, d) k(s, d)|: the sum of the
+    magnitudes of every term of I[t, s], which bounds the rounding error of
+    forming I in float32 (A22)."""
+    M = q_fp4.shape[0]
+    Q = np.abs(decode_mxfp4(q_fp4.reshape(M * INDEXER_HEADS, HEAD_DIM // 2),
+                            q_sf.reshape(M * INDEXER_HEADS, HEAD_DIM // FP4_BLOCK))).reshape(M, INDEXER_HEADS, HEAD_DIM)
+    K = np.abs(decode_mxfp4(k_fp4, k_sf))
+    return np.einsum("mh,mhn->mn", np.abs(np.asarray(weights, np.float64)), np.einsum("mhd,nd->mhn", Q, K))
+
+
+def indexer_topk(scores: np.ndarray, lengths: np.ndarray, k: int) -> np.ndarray:
+    """A21: per row t, the k keys s < L[t] with the largest scores (ties to
+    the smaller index), as int32 indices in ascending order, -1 padded."""
+    M = scores.shape[0]
+    out = np.full((M, k), -1, dtype=np.int32)
+    for t in range(M):
+        L = int(min(max(lengths[t], 0), scores.shape[1]))
+        idx = np.arange(L)
+        order = np.lexsort((idx, -np.asarray(scores[t, :L], np.float64)))   # score descending, then index
+        chosen = np.sort(order[:k])
+        out[t, :len(chosen)] = chosen
+    return out
