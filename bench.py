@@ -190,6 +190,16 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def clocks_max_mhz(gpu_index: int) -> float:
+    """The GPU's maximum SM clock (nvidia-smi), else the GB300 figure 2070."""
+    try:
+        out = subprocess.run(["nvidia-smi", f"--id={gpu_index}", "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10).stdout
+        return float(out.strip().splitlines()[0])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return 2070.0
+
+
 def cublas_fp8_tflops(dev, n: int = 8192, reps: int = 20):
     """Dense FP8 (E4M3 x E4M3 -> BF16, per-tensor scales) throughput of the
     vendor library on an n^3 GEMM, best of `reps` launches: a measured FP8
@@ -627,6 +637,56 @@ def run_ours(args):
     best_q = max([q_gbs] + [v["quant7168_gbs"] for v in sweep.values()])
     quantizer["roofline"]["best_kernel_gbs_in_run"] = best_q
     quantizer["roofline"]["frac_of_best_in_run"] = q_gbs / best_q
+    # ------------------------------------------- downstream indexer consumer
+    # The prefill step's FP4 Q (4632 tokens) scored against a 4632-key cache
+    # with causal visibility (query t sees keys s <= t), then the top-2048
+    # keys per query.  Each timed launch after an L2 flush.  The logits
+    # kernel is bound by its per-(query, key, head) epilogue arithmetic (a
+    # ReLU and a weighted add: 1.5 FP32 lane operations with packed FMAs);
+    # the top-k kernel by reading the scores.
+    indexer = {}
+    k_np, ks_np = W.indexer_keys(M, seed=5)
+    w_np = W.indexer_weights(M, seed=6)
+    kdev, ksdev, wdev = (torch.from_numpy(a).to(dev) for a in (k_np, ks_np, w_np))
+    len_dev = (torch.from_numpy(pos).to(dev) + 1).to(torch.int32)
+    q_idx, s_idx = chain_sets[0]["q"], chain_sets[0]["s"]
+    iq.prepare_q(chain_sets[0]["lat"], w0, ws, chain_sets[0]["p"], q_fp4=q_idx, q_sf=s_idx,
+                 workspace=chain_sets[0]["work"])
+    logits_buf = torch.empty((M, M), dtype=torch.float32, device=dev)
+    topk_buf = torch.empty((M, 2048), dtype=torch.int32, device=dev)
+    run_l = lambda i: iq.indexer_logits(q_idx, s_idx, kdev, ksdev, wdev, len_dev, logits=logits_buf)
+    run_t = lambda i: iq.indexer_topk(logits_buf, len_dev, 2048, indices=topk_buf)
+    for _ in range(3):
+        run_l(0)
+        run_t(0)
+    il_ms = flushed_ms(None, run_l, 30)
+    it_ms = flushed_ms(None, run_t, 30)
+    ib_ms = flushed_ms(None, lambda i: (run_l(i), run_t(i)), 30)
+    visible = int(len_dev.clamp(max=M).sum().item())
+    pair_heads = visible * 64
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_lane_ops_per_s = sm_count * 128 * (clocks_max_mhz(local) * 1e6)
+    alu_peak_pair_heads = alu_lane_ops_per_s / 1.5
+    l_avg = sum(il_ms) / len(il_ms)
+    t_avg = sum(it_ms) / len(it_ms)
+    indexer = {
+        "workload": "4632 queries (the prefill step's FP4 Q) x 4632 cached FP4 keys, causal, top-2048",
+        "visible_pairs": visible,
+        "logits_us": l_avg * 1e3, "topk_us": t_avg * 1e3, "both_us": sum(ib_ms) / len(ib_ms) * 1e3,
+        "logits_roofline": {"kernel": "indexer_logits_kernel", "bound": "alu",
+                            "achieved": pair_heads / (l_avg * 1e-3) / 1e12, "unit": "T pair-heads/s",
+                            "peak": alu_peak_pair_heads / 1e12,
+                            "frac": pair_heads / (l_avg * 1e-3) / alu_peak_pair_heads,
+                            "peak_source": f"{sm_count} SMs x 128 FP32 lanes x max SM clock, 1.5 lane ops per "
+                                           f"(query, key, head)",
+                            "fp4_tflops": visible * 64 * 128 * 2 / (l_avg * 1e-3) / 1e12},
+        "topk_roofline": {"kernel": "indexer_topk_kernel", "bound": "hbm",
+                          "achieved": visible * 4 / (t_avg * 1e-3) / 1e9, "unit": "GB/s", "peak": hbm_peak,
+                          "frac": visible * 4 / (t_avg * 1e-3) / 1e9 / hbm_peak,
+                          "bytes": "the visible scores, read once"},
+    }
+    del logits_buf, topk_buf
+
     # ------------------------------------------ end to end through the C ABI
     # iq_prepare_q_host on page-locked host buffers: every step reads the
     # latent rows and positions from host memory and returns the FP4 codes and
@@ -682,7 +742,7 @@ def run_ours(args):
             "clocks": clocks.summary(),
             "k1_chain_avg_ms": k1_avg_ms, "wall_s_timed": t_wall, "step_stats": step_stats,
             "back_to_back": back_to_back,
-            "decode": decode, "sweep": sweep, "fp4_formats": fp4_formats,
+            "decode": decode, "sweep": sweep, "fp4_formats": fp4_formats, "indexer": indexer,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

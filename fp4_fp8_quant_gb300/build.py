@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libiq.so")
 
-SOURCES = ["iq_api.cu", "iq_quant.cu", "iq_gemm.cu", "iq_small_m.cu"]
+SOURCES = ["iq_api.cu", "iq_quant.cu", "iq_gemm.cu", "iq_small_m.cu", "iq_indexer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -79,7 +79,7 @@ iq_status device_setup(int* max_pairs, int* sm_count = nullptr) {
     } else if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
       status = IQ_ERR_CUDA;
     } else if (iq::gemm_setup_device(&pairs) != cudaSuccess || pairs < 1 ||
-               iq::small_m_setup_device() != cudaSuccess) {
+               iq::small_m_setup_device() != cudaSuccess || iq::indexer_setup_device() != cudaSuccess) {
       status = IQ_ERR_CUDA;
     }
     if (status == IQ_OK && g_encode_tiled == nullptr) {
@@ -229,10 +229,11 @@ const char* iq_status_str(iq_status s) {
 }
 
 iq_status iq_device_status(uint32_t* flags, int reset) {
-  uint32_t v = 0, w = 0;
-  if (iq::read_device_status(&v, reset != 0) != cudaSuccess || iq::read_small_m_status(&w, reset != 0) != cudaSuccess)
+  uint32_t v = 0, w = 0, x = 0;
+  if (iq::read_device_status(&v, reset != 0) != cudaSuccess || iq::read_small_m_status(&w, reset != 0) != cudaSuccess ||
+      iq::read_indexer_status(&x, reset != 0) != cudaSuccess)
     return IQ_ERR_CUDA;
-  v |= w;
+  v |= w | x;
   if (flags) *flags = v;
   return v ? IQ_ERR_TIMEOUT : IQ_OK;
 }
@@ -629,4 +630,46 @@ extern "C" iq_status iq_prepare_q_host(const void* latent_bf16, int M, const voi
                       cudaStreamWaitEvent(stream, h.join, 0) == cudaSuccess;
   if (st != IQ_OK) return st;
   return ok && joined ? IQ_OK : IQ_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Downstream indexer: scores and top-k selection.
+
+extern "C" iq_status iq_indexer_logits(const uint8_t* q_fp4, const uint8_t* q_sf, int M, const uint8_t* k_fp4,
+                                       const uint8_t* k_sf, int N, const float* weights, const int32_t* lengths,
+                                       float* logits, long long ld_logits, cudaStream_t stream) {
+  if (M < 0 || N < 0) return IQ_ERR_ARG;
+  if (M == 0 || N == 0) return IQ_OK;
+  if (!q_fp4 || !q_sf || !k_fp4 || !k_sf || !weights || !lengths || !logits || ld_logits < N) return IQ_ERR_ARG;
+  if (!aligned(q_fp4, 16) || !aligned(k_fp4, 16) || !aligned(q_sf, 16) || !aligned(k_sf, 16) || !aligned(weights, 16) ||
+      !aligned(lengths, 4) || !aligned(logits, 4)) {
+    return IQ_ERR_ALIGN;
+  }
+  if (static_cast<long long>(M) * iq::kNumHeads > (1ll << 31) - 1) return IQ_ERR_ARG;
+  int max_pairs = 0, sm_count = 0;
+  const iq_status st = device_setup(&max_pairs, &sm_count);
+  if (st != IQ_OK) return st;
+  CUtensorMap tm_k, tm_q;
+  if (!encode_2d_u8(&tm_k, k_fp4, iq::kHeadDim / 2, static_cast<uint64_t>(N), 64, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_2d_u8(&tm_q, q_fp4, iq::kHeadDim / 2, static_cast<uint64_t>(M) * iq::kNumHeads, 64, 128,
+                    CU_TENSOR_MAP_SWIZZLE_64B)) {
+    return IQ_ERR_CUDA;
+  }
+  return iq::launch_indexer_logits(tm_k, tm_q, q_sf, k_sf, weights, lengths, logits, ld_logits, M, N, sm_count,
+                                   g_timeout_ns.load(std::memory_order_relaxed), stream) == cudaSuccess
+             ? IQ_OK
+             : IQ_ERR_CUDA;
+}
+
+extern "C" iq_status iq_indexer_topk(const float* logits, long long ld_logits, int M, int N, const int32_t* lengths,
+                                     int k, int32_t* indices, cudaStream_t stream) {
+  if (M < 0 || N < 0 || k < 1) return IQ_ERR_ARG;
+  if (M == 0) return IQ_OK;
+  if (!logits || !lengths || !indices || ld_logits < N) return IQ_ERR_ARG;
+  if (!aligned(logits, 4) || !aligned(lengths, 4) || !aligned(indices, 4)) return IQ_ERR_ALIGN;
+  int max_pairs = 0;
+  const iq_status st = device_setup(&max_pairs);
+  if (st != IQ_OK) return st;
+  return iq::launch_indexer_topk(logits, ld_logits, M, N, lengths, k, indices, stream) == cudaSuccess ? IQ_OK
+                                                                                                      : IQ_ERR_CUDA;
 }

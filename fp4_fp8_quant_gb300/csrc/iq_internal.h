@@ -108,4 +108,15 @@ cudaError_t launch_small_m_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUte
 cudaError_t read_device_status(uint32_t* flags, bool reset);
 cudaError_t read_small_m_status(uint32_t* flags, bool reset);
 
+// The downstream indexer: scores of (query, key) pairs and top-k selection.
+// q_fp4 / k_fp4 are read through the tensor maps tm_q ([M * 64, 64] bytes)
+// and tm_k ([N, 64] bytes), 64-byte boxes of 128 rows, 64-byte swizzle.
+cudaError_t indexer_setup_device();
+cudaError_t launch_indexer_logits(const CUtensorMap& tm_k, const CUtensorMap& tm_q, const uint8_t* q_sf,
+                                  const uint8_t* k_sf, const float* w, const int32_t* len, float* logits, long long ld,
+                                  int M, int N, int sm_count, unsigned long long timeout_ns, cudaStream_t stream);
+cudaError_t launch_indexer_topk(const float* logits, long long ld, int M, int N, const int32_t* len, int k,
+                                int32_t* out, cudaStream_t stream);
+cudaError_t read_indexer_status(uint32_t* flags, bool reset);
+
 }  // namespace iq

@@ -114,6 +114,25 @@ __device__ __forceinline__ void tma_store_wait_read() {
 // Waits until every committed bulk store of this thread has completed.
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// 4- or 16-byte asynchronous copy global -> shared (cp.async, L2 only for 16
+// bytes); src_bytes < bytes fills the rest with zeros (0: nothing is read).
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most n of this thread's committed cp.async groups are pending.
+template <int n>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
+}
+
 // ----------------------------------------- programmatic dependent launch
 
 // Blocks until the grids this grid depends on (the preceding kernel of the
@@ -359,6 +378,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor of a K-major operand tile stored with the
+// 64-byte swizzle: rows of 64 bytes (128 packed FP4 values), 8-row core groups
+// 512 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;            // leading byte offset (unused with this swizzle)
+  d |= static_cast<uint64_t>(512 >> 4) << 32;     // stride byte offset: 8 rows x 64 B
+  d |= static_cast<uint64_t>(1) << 46;            // descriptor version for tcgen05
+  d |= static_cast<uint64_t>(4) << 61;            // 64-byte swizzle
+  return d;
+}
+
 // Descriptor of an unswizzled 32-row x 16-byte scale-factor tile (8-row core
 // groups 128 bytes apart), the source of tcgen05.cp 32x128b.
 __device__ __forceinline__ uint64_t smem_desc_sf(uint32_t saddr) {
@@ -374,6 +405,27 @@ __device__ __forceinline__ uint64_t smem_desc_sf(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, int sfa_id, int sfb_id) {
   return (static_cast<uint32_t>(sfb_id) << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sfa_id) << 29);
+}
+
+// Instruction descriptor of kind::mxf4 with block scaling: E2M1 A and B
+// (packed two per byte), both K-major, FP32 accumulate, UE8M0 scales, one per
+// 32 K (scale_vec::2X: an MMA of K = 64 reads two bytes of each row's scale
+// word, from byte sfa_id / sfb_id, which is 0 or 2).
+__host__ __device__ constexpr uint32_t idesc_mxf4_e2m1(int M, int N, int sfa_id, int sfb_id) {
+  return (static_cast<uint32_t>(sfb_id) << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sfa_id) << 29);
+}
+
+// D(tmem) (+)= A(smem) * B(smem)^T, E2M1 x E2M1 -> FP32, with per-32-K UE8M0
+// scales of A rows and B rows read from TMEM (K = 64 per instruction).
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
 }
 
 // --------------------------------------------------------------- conversions

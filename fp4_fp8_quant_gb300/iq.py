@@ -51,6 +51,8 @@ SIGNATURES = {
     "iq_prepare_q_host": (_I, [_P, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P]),
     "iq_set_host_chunk_rows": (_I, [_I]),
     "iq_host_chunk_rows": (_I, []),
+    "iq_indexer_logits": (_I, [_P, _P, _I, _P, _P, _I, _P, _P, _P, ctypes.c_longlong, _P]),
+    "iq_indexer_topk": (_I, [_P, ctypes.c_longlong, _I, _I, _P, _I, _P, _P]),
 }
 
 # FP4 output variants (include/iq.h, iq_fp4_format).
@@ -307,3 +309,46 @@ def set_small_m_threshold(max_tokens: int) -> int:
 
 def small_m_threshold() -> int:
     return int(lib().iq_small_m_threshold())
+
+
+def indexer_logits(q_fp4: torch.Tensor, q_sf: torch.Tensor, k_fp4: torch.Tensor, k_sf: torch.Tensor,
+                   weights: torch.Tensor, lengths: torch.Tensor, *, logits: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """Indexer scores (include/iq.h, iq_indexer_logits): q_fp4 uint8 [M, 4096],
+    q_sf uint8 [M, 256], k_fp4 uint8 [N, 64], k_sf uint8 [N, 4], weights
+    float32 [M, 64], lengths int32 [M] -> logits float32 [M, N] (row stride may
+    exceed N); entries at s >= lengths[t] are left as they were."""
+    M, N = q_fp4.shape[0], k_fp4.shape[0]
+    _require(q_fp4, "q_fp4", (torch.uint8,), (M, Q_DIM // 2))
+    _require(q_sf, "q_sf", (torch.uint8,), (M, Q_DIM // 32))
+    _require(k_fp4, "k_fp4", (torch.uint8,), (N, HEAD_DIM // 2))
+    _require(k_sf, "k_sf", (torch.uint8,), (N, HEAD_DIM // 32))
+    _require(weights, "weights", (torch.float32,), (M, N_HEADS))
+    _require(lengths, "lengths", (torch.int32,), (M,))
+    if logits is None:
+        logits = torch.empty((M, N), dtype=torch.float32, device=q_fp4.device)
+    if logits.dim() != 2 or logits.shape[0] != M or logits.shape[1] < N or logits.stride(1) != 1:
+        raise ValueError("logits must be float32 [M, >= N] with unit column stride")
+    _require(logits, "logits", (torch.float32,), contiguous=False)
+    _check(lib().iq_indexer_logits(_ptr(q_fp4), _ptr(q_sf), M, _ptr(k_fp4), _ptr(k_sf), N, _ptr(weights),
+                                   _ptr(lengths), _ptr(logits), logits.stride(0), _stream(stream)),
+           "iq_indexer_logits")
+    return logits
+
+
+def indexer_topk(logits: torch.Tensor, lengths: torch.Tensor, k: int, *, N: int | None = None,
+                 indices: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Top-k key selection per query row (include/iq.h, iq_indexer_topk):
+    int32 [M, k] ascending indices, -1 padded.  N defaults to logits.shape[1]."""
+    M = logits.shape[0]
+    N = logits.shape[1] if N is None else N
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a 2-D tensor with unit column stride")
+    _require(logits, "logits", (torch.float32,), contiguous=False)
+    _require(lengths, "lengths", (torch.int32,), (M,))
+    if indices is None:
+        indices = torch.empty((M, k), dtype=torch.int32, device=logits.device)
+    _require(indices, "indices", (torch.int32,), (M, k))
+    _check(lib().iq_indexer_topk(_ptr(logits), logits.stride(0), M, N, _ptr(lengths), int(k), _ptr(indices),
+                                 _stream(stream)), "iq_indexer_topk")
+    return indices

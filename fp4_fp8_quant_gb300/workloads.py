@@ -192,3 +192,15 @@ def indexer_inputs(M: int, N: int, seed: int = 0, causal: bool = True):
     else:
         lengths = np.full(M, N, np.int32)
     return q, q_sf, k, k_sf, w, lengths
+
+
+def indexer_keys(N: int, seed: int = 0):
+    """A key cache alone: codes [N, 64] and UE8M0 scale bytes [N, 4], drawn as
+    in indexer_inputs."""
+    rng = _rng(4000 + seed)
+    return mxfp4_codes(N, HEAD_DIM, rng), rng.integers(122, 127, size=(N, HEAD_DIM // 32)).astype(np.uint8)
+
+
+def indexer_weights(M: int, seed: int = 0) -> np.ndarray:
+    """Per-head weights alone: float32 [M, 64], N(0, 1/64)."""
+    return (_rng(5000 + seed).standard_normal((M, N_HEADS)) / 8).astype(np.float32)

@@ -367,6 +367,47 @@ iq_status iq_prepare_q_host(const void* latent_bf16, int M,
 int iq_set_host_chunk_rows(int rows);
 int iq_host_chunk_rows(void);
 
+/* ------------------------------------------------------------------------
+ * 3. The consumer of the prepared Q: the sparse-attention indexer's scores
+ *    and top-k key selection (the TokenSpeed PR names the indexer top-k and
+ *    writes it straight to its destination -- Summary; Prefill host-sync
+ *    cleanup -- but gives neither formula nor layout; these are this
+ *    library's readings).
+ *
+ *   score  I[t, s] = sum over heads h < 64 of w[t, h] * max(0, q(t, h) . k(s))
+ *          q(t, h): head h of query token t, decoded from the MXFP4 Q that
+ *            iq_prepare_q writes (q_fp4 [M, 4096], q_sf [M, 256]);
+ *          k(s): the 128-dim key of cached token s, in the same MXFP4 format
+ *            (k_fp4 [N, 64] bytes: element 2i in the low nibble of byte i;
+ *            k_sf [N, 4] UE8M0 bytes, byte b for dims 32 b .. 32 b + 31);
+ *          w: float32 [M, 64] per-head weights of each query token;
+ *          keys s < L[t] are visible to query t (L: int32 [M], clamped to
+ *            [0, N]; causal prefill passes position + 1).
+ *   The head dot products are accumulated in float32 by the tensor cores;
+ *   the ReLU and the weighted head sum are float32.
+ * ------------------------------------------------------------------------ */
+
+/* Writes logits[t * ld_logits + s] = I[t, s] for every visible pair (s <
+ * L[t]); entries s >= L[t] are not written.  One kernel launch.
+ * Requirements: M, N >= 0 (M == 0 or N == 0: IQ_OK, no launch); ld_logits >=
+ * N; q_fp4, q_sf, k_fp4, k_sf and weights 16-byte aligned, lengths and
+ * logits 4-byte aligned (else IQ_ERR_ALIGN); M * 64 < 2^31 (else IQ_ERR_ARG).
+ * Launched as a programmatic dependent of the preceding kernel: nothing is
+ * read before that kernel completes. */
+iq_status iq_indexer_logits(const uint8_t* q_fp4, const uint8_t* q_sf, int M, const uint8_t* k_fp4,
+                            const uint8_t* k_sf, int N, const float* weights, const int32_t* lengths,
+                            float* logits, long long ld_logits, cudaStream_t stream);
+
+/* For every query row t: the k visible keys (s < L[t]) with the largest
+ * logits[t * ld_logits + s], ties to the smaller index (-0 and +0 tie), as
+ * int32 indices in ascending order in indices[t * k .. t * k + k - 1], padded
+ * with -1 when fewer than k keys are visible.  Scores must not be NaN.  One
+ * kernel launch (one block per row), a programmatic dependent of the
+ * preceding kernel (normally iq_indexer_logits).  Requirements: k >= 1,
+ * ld_logits >= N, 4-byte aligned pointers. */
+iq_status iq_indexer_topk(const float* logits, long long ld_logits, int M, int N, const int32_t* lengths, int k,
+                          int32_t* indices, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -153,3 +153,55 @@ def check_fp4(gpu_q, gpu_sf, ora_q, ora_sf, ora_z, min_equal=0.9999, fmt="mx"):
     return {"scale_mismatch_blocks": int(sf_diff.sum()), "code_mismatches": n_code,
             "signed_zero_flips": n_zero_flip,
             "equal_fraction": frac_equal, "worst_boundary_rel": worst_rel}
+
+
+# ---------------------------------------------------- downstream indexer rules
+#
+# Logits: |gpu - oracle| <= 2^-16 * S[t, s] for every visible pair, where S is
+# the sum of the magnitudes of every term of the score (the oracle's
+# indexer_logit_magnitude): the float32 accumulation of the 128-term head dot
+# products, the ReLU and the 64-term weighted sum stays within ~200 float32
+# roundings of S.
+# Top-k: bit-exact against the oracle's selection applied to the GPU's own
+# scores (the selection itself is exact); against the oracle's float64 scores
+# the chosen sets may differ only at keys whose score is within the logits
+# tolerance of the oracle's k-th largest score.
+
+LOGIT_TOL = 2.0 ** -16
+
+
+def check_logits(gpu, ora, mag, lengths):
+    gpu = np.asarray(gpu, np.float64)
+    worst = 0.0
+    for t in range(ora.shape[0]):
+        L = int(min(max(lengths[t], 0), ora.shape[1]))
+        if L == 0:
+            continue
+        err = np.abs(gpu[t, :L] - ora[t, :L])
+        bound = LOGIT_TOL * mag[t, :L] + 1e-30
+        assert np.all(err <= bound), f"row {t}: logit error {float((err / bound).max()):.3g} x the bound"
+        worst = max(worst, float((err / (mag[t, :L] + 1e-30)).max()))
+    return worst
+
+
+def check_topk_vs_oracle_scores(gpu_idx, ora_scores, mag, lengths, k):
+    """Chosen sets equal except at keys within the logits tolerance of the
+    oracle's k-th largest score.  Returns the number of rows whose sets differ."""
+    rows_differing = 0
+    for t in range(ora_scores.shape[0]):
+        L = int(min(max(lengths[t], 0), ora_scores.shape[1]))
+        g = set(int(i) for i in gpu_idx[t] if i >= 0)
+        assert len(g) == min(L, k) and all(i < L for i in g), f"row {t}: bad selection size or index"
+        if L <= k:
+            assert g == set(range(L))
+            continue
+        s = ora_scores[t, :L]
+        kth = np.sort(s)[::-1][k - 1]
+        near = np.abs(s - kth) <= 2 * LOGIT_TOL * mag[t, :L] + 1e-30
+        must = set(np.nonzero((s > kth) & ~near)[0].tolist())
+        must_not = set(np.nonzero((s < kth) & ~near)[0].tolist())
+        assert must <= g, f"row {t}: {len(must - g)} keys clearly above the threshold not chosen"
+        assert not (must_not & g), f"row {t}: {len(must_not & g)} keys clearly below the threshold chosen"
+        ora_set = set(np.sort(np.lexsort((np.arange(L), -s))[:k]).tolist())
+        rows_differing += int(g != ora_set)
+    return rows_differing
