@@ -32,8 +32,10 @@
 //
 // K6 indexer_topk_kernel.  One CTA per query row: radix selection of the k-th
 // largest score over order-preserving 32-bit keys (11, 11, then 10 bits,
-// histograms in shared memory), then one pass in index order that writes the
-// keys above the threshold and the first (smallest-index) keys equal to it.
+// histograms in shared memory; a row of up to 12288 keys is read once and
+// kept in shared memory), then a pass in index order over contiguous
+// per-thread segments that writes the keys above the threshold and the first
+// (smallest-index) keys equal to it.
 //
 // Every mbarrier wait is bounded (timeout_ns); a wait that gives up records
 // its kind in this file's status word and raises a CTA abort flag.
@@ -388,7 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------- top-k
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 256;
+constexpr int kTopkCacheMax = 12288;   // rows up to this many keys are read once, into shared memory
 
 // Order-preserving key of a float score (larger score -> larger key); -0 is
 // taken as +0 so that the two zeros tie and the smaller index wins.
@@ -411,13 +414,13 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* s
   if (lane == 31) scratch[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t s = lane < kTopkThreads / 32 ? scratch[lane] : 0u;
+    uint32_t t = lane < kTopkThreads / 32 ? scratch[lane] : 0u;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, s, d);
-      if (lane >= d) s += y;
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, t, d);
+      if (lane >= d) t += y;
     }
-    if (lane < kTopkThreads / 32) scratch[lane] = s;   // inclusive over warps
+    if (lane < kTopkThreads / 32) scratch[lane] = t;   // inclusive over warps
   }
   __syncthreads();
   const uint32_t before = warp > 0 ? scratch[warp - 1] : 0u;
@@ -426,35 +429,18 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* s
   return before + x - v;
 }
 
-// Among the keys that match `prefix` on the bits above `shift + bits`, the
-// digit (bits [shift, shift + bits)) that holds the rank-th largest key (rank
-// counted from 1 among the matching keys); *above gets the number of matching
+// The digit d (of the histogram's nb bins, largest first) that holds the
+// rank-th largest of the counted keys (rank from 1), and *above = the count of
 // keys with a larger digit.
-__device__ uint32_t select_digit(const float* row, int L, uint32_t prefix, int hi_shift, int shift, int bits,
-                                 uint32_t rank, uint32_t* hist, uint32_t* scratch, uint32_t* above) {
-  const int nb = 1 << bits;
-  for (int i = threadIdx.x; i < nb; i += kTopkThreads) hist[i] = 0u;
-  __syncthreads();
-  for (int i = threadIdx.x; i < L; i += kTopkThreads) {
-    const uint32_t k = score_key(row[i]);
-    if (hi_shift >= 32 || (k >> hi_shift) == prefix) atomicAdd(&hist[(k >> shift) & (nb - 1)], 1u);
-  }
-  __syncthreads();
-  // Suffix sums from the largest digit down, per thread over a run of bins.
-  const int per = nb / kTopkThreads > 0 ? nb / kTopkThreads : 1;
+__device__ uint32_t find_digit(const uint32_t* hist, int nb, uint32_t rank, uint32_t* scratch, uint32_t* above) {
+  __shared__ uint32_t found_digit, found_above;
+  const int per = nb / kTopkThreads;
   const int first = nb - (threadIdx.x + 1) * per;   // thread 0 takes the largest digits
   uint32_t run = 0;
-  if (first >= 0)
-    for (int j = 0; j < per; ++j) run += hist[first + j];
+  for (int j = 0; j < per; ++j) run += hist[first + j];
   uint32_t total;
   const uint32_t before = block_exclusive_scan(run, scratch, &total);   // keys with larger digits
-  __shared__ uint32_t found_digit, found_above;
-  if (threadIdx.x == 0) {
-    found_digit = 0u;
-    found_above = 0u;
-  }
-  __syncthreads();
-  if (first >= 0 && before < rank && rank <= before + run) {
+  if (before < rank && rank <= before + run) {
     uint32_t acc = before;
     for (int j = per - 1; j >= 0; --j) {
       const uint32_t c = hist[first + j];
@@ -471,9 +457,14 @@ __device__ uint32_t select_digit(const float* row, int L, uint32_t prefix, int h
   return found_digit;
 }
 
+// K6: per query row t, the k visible keys with the largest scores (see the
+// file comment).  Rows of at most kTopkCacheMax visible keys are read from
+// global memory once, as order-preserving keys into shared memory; longer
+// rows are read again by every pass.
 __global__ void __launch_bounds__(kTopkThreads)
     indexer_topk_kernel(const float* __restrict__ logits, long long ld, int N, const int32_t* __restrict__ len,
-                        int k, int32_t* __restrict__ out) {
+                        int k, int32_t* __restrict__ out, int cache_keys) {
+  extern __shared__ uint32_t cache[];   // cache_keys words
   __shared__ uint32_t hist[2048];
   __shared__ uint32_t scratch[kTopkThreads / 32];
   // The scores are the preceding kernel's output.
@@ -487,37 +478,73 @@ __global__ void __launch_bounds__(kTopkThreads)
     for (int i = threadIdx.x; i < k; i += kTopkThreads) dst[i] = i < L ? i : -1;
     return;
   }
-  // Threshold key T = the k-th largest: 11 + 11 + 10 bits.
+  const bool cached = L <= cache_keys;
+  auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : score_key(row[i]); };
+
+  // Digit 1: bits 31..21 (read the row, cache it).
+  for (int i = threadIdx.x; i < 2048; i += kTopkThreads) hist[i] = 0u;
+  __syncthreads();
+  for (int i = threadIdx.x; i < L; i += kTopkThreads) {
+    const uint32_t key = score_key(row[i]);
+    if (cached) cache[i] = key;
+    atomicAdd(&hist[key >> 21], 1u);
+  }
+  __syncthreads();
   uint32_t above1, above2, above3;
-  const uint32_t d1 = select_digit(row, L, 0u, 32, 21, 11, static_cast<uint32_t>(k), hist, scratch, &above1);
-  const uint32_t d2 =
-      select_digit(row, L, d1, 21, 10, 11, static_cast<uint32_t>(k) - above1, hist, scratch, &above2);
-  const uint32_t d3 = select_digit(row, L, (d1 << 11) | d2, 10, 0, 10, static_cast<uint32_t>(k) - above1 - above2,
-                                   hist, scratch, &above3);
-  const uint32_t T = (d1 << 21) | (d2 << 10) | d3;
+  const uint32_t d1 = find_digit(hist, 2048, static_cast<uint32_t>(k), scratch, &above1);
+  // Digit 2: bits 20..10 of the keys with digit 1 = d1.
+  for (int i = threadIdx.x; i < 2048; i += kTopkThreads) hist[i] = 0u;
+  __syncthreads();
+  for (int i = threadIdx.x; i < L; i += kTopkThreads) {
+    const uint32_t key = key_at(i);
+    if ((key >> 21) == d1) atomicAdd(&hist[(key >> 10) & 0x7FFu], 1u);
+  }
+  __syncthreads();
+  const uint32_t d2 = find_digit(hist, 2048, static_cast<uint32_t>(k) - above1, scratch, &above2);
+  // Digit 3: bits 9..0 of the keys with digits (d1, d2).
+  for (int i = threadIdx.x; i < 1024; i += kTopkThreads) hist[i] = 0u;
+  __syncthreads();
+  const uint32_t hi22 = (d1 << 11) | d2;
+  for (int i = threadIdx.x; i < L; i += kTopkThreads) {
+    const uint32_t key = key_at(i);
+    if ((key >> 10) == hi22) atomicAdd(&hist[key & 0x3FFu], 1u);
+  }
+  __syncthreads();
+  const uint32_t d3 = find_digit(hist, 1024, static_cast<uint32_t>(k) - above1 - above2, scratch, &above3);
+  const uint32_t T = (hi22 << 10) | d3;
   const uint32_t n_above = above1 + above2 + above3;            // keys > T
   const uint32_t n_equal = static_cast<uint32_t>(k) - n_above;  // keys == T to take, smallest index first
-  // One pass in index order: position of each chosen key = chosen keys before it.
-  uint32_t base = 0, eq_base = 0;
-  for (int i0 = 0; i0 < L; i0 += kTopkThreads) {
-    const int i = i0 + threadIdx.x;
-    const uint32_t key = i < L ? score_key(row[i]) : 0u;
-    const uint32_t gt = i < L && key > T ? 1u : 0u;
-    const uint32_t eq = i < L && key == T ? 1u : 0u;
-    uint32_t eq_total, sel_total;
-    const uint32_t eq_before = eq_base + block_exclusive_scan(eq, scratch, &eq_total);
-    const uint32_t sel = gt | (eq && eq_before < n_equal ? 1u : 0u);
-    const uint32_t pos = base + block_exclusive_scan(sel, scratch, &sel_total);
-    if (sel) dst[pos] = i;
-    base += sel_total;
-    eq_base += eq_total;
+
+  // Output: thread i takes the contiguous segment [i seg, (i + 1) seg); one
+  // scan of its counts gives where its chosen keys go.
+  const int seg = (L + kTopkThreads - 1) / kTopkThreads;
+  const int b = threadIdx.x * seg;
+  const int e = min(L, b + seg);
+  uint32_t gt = 0, eq = 0;
+  for (int i = b; i < e; ++i) {
+    const uint32_t key = key_at(i);
+    gt += key > T ? 1u : 0u;
+    eq += key == T ? 1u : 0u;
+  }
+  uint32_t tot;
+  const uint32_t gt_before = block_exclusive_scan(gt, scratch, &tot);
+  uint32_t eq_before = block_exclusive_scan(eq, scratch, &tot);
+  uint32_t pos = gt_before + min(eq_before, n_equal);
+  for (int i = b; i < e; ++i) {
+    const uint32_t key = key_at(i);
+    if (key > T || (key == T && eq_before < n_equal)) dst[pos++] = i;
+    if (key == T) ++eq_before;
   }
 }
 
 }  // namespace
 
 cudaError_t indexer_setup_device() {
-  return cudaFuncSetAttribute(indexer_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const cudaError_t err =
+      cudaFuncSetAttribute(indexer_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err != cudaSuccess) return err;
+  return cudaFuncSetAttribute(indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kTopkCacheMax * static_cast<int>(sizeof(uint32_t)));
 }
 
 cudaError_t launch_indexer_logits(const CUtensorMap& tm_k, const CUtensorMap& tm_q, const uint8_t* q_sf,
@@ -556,14 +583,18 @@ cudaError_t launch_indexer_topk(const float* logits, long long ld, int M, int N,
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  // Shared memory for the row cache: enough for N keys, at most the cap
+  // (longer rows are streamed from global memory by every pass).
+  const int cache_keys = N < kTopkCacheMax ? N : kTopkCacheMax;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(M, 1, 1);
   cfg.blockDim = dim3(kTopkThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = static_cast<size_t>(N <= kTopkCacheMax ? cache_keys : 0) * sizeof(uint32_t);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, indexer_topk_kernel, logits, ld, N, len, k, out);
+  return cudaLaunchKernelEx(&cfg, indexer_topk_kernel, logits, ld, N, len, k, out,
+                            N <= kTopkCacheMax ? cache_keys : 0);
 }
 
 cudaError_t read_indexer_status(uint32_t* flags, bool reset) {
