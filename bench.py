@@ -679,11 +679,12 @@ def run_ours(args):
                             "frac": pair_heads / (l_avg * 1e-3) / alu_peak_pair_heads,
                             "peak_source": f"{sm_count} SMs x 128 FP32 lanes x max SM clock, 1.5 lane ops per "
                                            f"(query, key, head)",
-                            "fp4_tflops": visible * 64 * 128 * 2 / (l_avg * 1e-3) / 1e12},
+                            "fp4_tflops": visible * 64 * 128 * 2 / (l_avg * 1e-3) / 1e12,
+                            "traffic": kernel_traffic("indexer_logits_kernel")},
         "topk_roofline": {"kernel": "indexer_topk_kernel", "bound": "hbm",
                           "achieved": visible * 4 / (t_avg * 1e-3) / 1e9, "unit": "GB/s", "peak": hbm_peak,
                           "frac": visible * 4 / (t_avg * 1e-3) / 1e9 / hbm_peak,
-                          "bytes": "the visible scores, read once"},
+                          "bytes": "the visible scores, read once", "traffic": kernel_traffic("indexer_topk_kernel")},
     }
     del logits_buf, topk_buf
 

@@ -4,11 +4,13 @@ profiles are taken with.
 
     python -m fp4_fp8_quant_gb300 prepare --tokens 4632 [--repeat 3] [--route auto|small|pair]
     python -m fp4_fp8_quant_gb300 quant --rows 4632 --cols 7168 [--repeat 3]
+    python -m fp4_fp8_quant_gb300 indexer --queries 4632 --keys 4632 [--topk 2048] [--full] [--repeat 3]
 
 `prepare` calls iq_prepare_q on the prefill workload when --tokens is 4632
 (positions 0..M-1) and on the decode workload otherwise (random positions);
-`quant` calls the FP8 1x128 quantizer on the blocks workload.  L2 is flushed
-before every call.
+`quant` calls the FP8 1x128 quantizer on the blocks workload; `indexer` scores
+random FP4 queries against a random FP4 key cache (causal unless --full) and
+selects the top-k keys per query.  L2 is flushed before every call.
 """
 
 from __future__ import annotations
@@ -52,6 +54,12 @@ def main(argv=None) -> int:
     q.add_argument("--rows", type=int, default=4632)
     q.add_argument("--cols", type=int, default=7168)
     q.add_argument("--repeat", type=int, default=3)
+    ix = sub.add_parser("indexer")
+    ix.add_argument("--queries", type=int, default=4632)
+    ix.add_argument("--keys", type=int, default=4632)
+    ix.add_argument("--topk", type=int, default=2048)
+    ix.add_argument("--full", action="store_true")
+    ix.add_argument("--repeat", type=int, default=3)
     args = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -73,6 +81,16 @@ def main(argv=None) -> int:
             if old is not None:
                 iq.set_small_m_threshold(old)
         print(f"prepare M={M} route={args.route}: " + " ".join(f"{u:.2f}" for u in us) + " us per call")
+    elif args.cmd == "indexer":
+        M, N = args.queries, args.keys
+        arrays = W.indexer_inputs(M, N, seed=1, causal=not args.full)
+        q4, qs, k4, ks, w, L = (torch.from_numpy(a).to(dev) for a in arrays)
+        logits = torch.empty((M, N), dtype=torch.float32, device=dev)
+        idx = torch.empty((M, args.topk), dtype=torch.int32, device=dev)
+        us_l = _time_calls(lambda: iq.indexer_logits(q4, qs, k4, ks, w, L, logits=logits), args.repeat, dev)
+        us_t = _time_calls(lambda: iq.indexer_topk(logits, L, args.topk, indices=idx), args.repeat, dev)
+        print(f"indexer {M}x{N} {'full' if args.full else 'causal'}: logits " + " ".join(f"{u:.2f}" for u in us_l)
+              + f" us; top-{args.topk} " + " ".join(f"{u:.2f}" for u in us_t) + " us per call")
     else:
         xb = W.quant_blocks_input(args.rows, args.cols, seed=1)
         X = _bf16(xb, dev)
