@@ -16,8 +16,9 @@
 // tensor memory receives the 128 x 256 FP32 accumulator of its own rows.  On
 // GB300 the 1-SM M = 128 MMA measured 1.3-1.6x slower per SM than this form,
 // which reaches the tensor-core peak.  K = 1536 streams as twelve 128-byte
-// K-blocks.  Each pair takes a contiguous run of tiles in feature-major order,
-// so consecutive tiles mostly share their two heads.
+// K-blocks.  Each pair takes a contiguous run of tiles, by default in
+// token-major order (consecutive tiles share their token rows); a one-head
+// tile width (128 features) is kept as an instance for measurements.
 // Warp roles (320 threads per CTA):
 //   warp 0      TMA producer (both CTAs): a 6-stage ring of {X 16 KB, W 16 KB},
 //               128-byte swizzled; each load signals the leader CTA's barrier.

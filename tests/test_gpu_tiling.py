@@ -1,8 +1,8 @@
 """The CTA-pair kernel's tilings: one head (128 features) or two heads (256)
 per pair tile, feature-major or token-major tile order.  Every setting
 computes each output with the same sums in the same order, so all of them must
-give the same bytes, and the default route (one head per tile up to 1024
-tokens) must match the oracle at the mid-size token counts."""
+give the same bytes, and the default route (two heads per tile, token-major
+order) must match the oracle at the mid-size token counts."""
 
 import contextlib
 
