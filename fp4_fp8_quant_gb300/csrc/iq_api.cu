@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr uint64_t kMaxQuantDelayNs = 1000000ull;   // diagnostics: at most 1 ms per wave
 
 struct DeviceInfo {
   bool ready = false;
@@ -34,7 +35,7 @@ std::atomic<int> g_fail_setups{0};   // test hook: set-ups to fail on purpose
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_small_m_max{iq::kSmallMMax};
 std::atomic<int> g_tile_n_override{0};   // 0: by token count; else 128 or 256
-std::atomic<int> g_order_override{0};    // 0: by token count; 1 feature-major; 2 token-major
+std::atomic<int> g_order_override{0};    // 0: default; 1 feature-major; 2 token-major; 3 interleaved
 
 // Tile width and order of the CTA-pair kernel.  Measured on GB300 (kernel
 // alone, L2 flushed, 65 ... 65536 tokens): the two-head tile is as fast as
@@ -47,9 +48,12 @@ int gemm_tile_n(int) {
   return o == 128 ? 128 : 256;
 }
 
-int gemm_token_major(int) {
-  const int o = g_order_override.load(std::memory_order_relaxed);
-  return o == 1 ? 0 : 1;
+int gemm_order(int) {
+  switch (g_order_override.load(std::memory_order_relaxed)) {
+    case 1: return iq::kOrderFeatureMajor;
+    case 3: return iq::kOrderInterleaved;
+    default: return iq::kOrderTokenMajor;
+  }
 }
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 
@@ -133,11 +137,34 @@ iq::RopeTurns make_rope_turns() {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Workspace of iq_prepare_q: the FP8 latent [M][1536], its packed scale
+// words [3][align4(M)], then the fused quantizer's flags (an epoch word and
+// one progress word per CTA, 8 bytes each), each region 256-byte aligned.
+size_t prepare_scales_offset(int M) { return align_up(static_cast<size_t>(M) * iq::kLatentDim, 256); }
+size_t prepare_counters_offset(int M) {
+  return align_up(prepare_scales_offset(M) +
+                      static_cast<size_t>(iq::kScaleGroups) * align_up(static_cast<size_t>(M), 4) * sizeof(int32_t),
+                  256);
+}
+
+// The quantizer fused into the CTA-pair kernel.  Off by default: measured on
+// GB300 the fused launch is slower than the two-launch chain at every token
+// count (76 against 50 us at 4632 tokens): the quantizing epilogue warps
+// become the pipeline's bottleneck and the first MMAs wait for the first
+// wave's rows.  On runs the fused launch (tests, measurements).
+std::atomic<int> g_quant_fusion{0};
+std::atomic<unsigned long long> g_quant_delay_ns{0};
+
+struct FusedQuant {
+  const void* latent;
+  unsigned long long* counters;
+};
+
 iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq, const uint8_t* wq_sf,
                      const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf, float* q_pre, int fmt, int max_pairs,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, const FusedQuant* fuse = nullptr) {
   static const iq::RopeTurns rope = make_rope_turns();
-  iq::GemmArgs a;
+  iq::GemmArgs a{};
   a.x_sf = x_sf;
   a.w_sf = wq_sf;
   a.pos = positions;
@@ -150,7 +177,7 @@ iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq,
   a.num_m_pairs = (a.num_m_tiles + iq::gemm_pair_size() - 1) / iq::gemm_pair_size();
   const int tile_n = gemm_tile_n(M);
   a.num_pair_tiles = a.num_m_pairs * (iq::kQDim / tile_n);
-  a.token_major = gemm_token_major(M);
+  a.order = gemm_order(M);
   a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
   a.rope = rope;
   CUtensorMap tm_x, tm_w, tm_q;
@@ -170,6 +197,16 @@ iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq,
                     static_cast<uint32_t>(tile_n / iq::gemm_pair_size())) ||
       !encode_2d_u8(&tm_q, q_fp4, iq::kQDim / 2, static_cast<uint64_t>(M), 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) {
     return IQ_ERR_CUDA;
+  }
+  if (fuse != nullptr) {
+    a.order = iq::kOrderInterleaved;
+    a.latent = static_cast<const uint16_t*>(fuse->latent);
+    a.x_fp8 = static_cast<uint8_t*>(const_cast<void*>(xq));
+    a.x_sf_out = const_cast<int32_t*>(x_sf);
+    a.ready = fuse->counters;
+    a.quant_delay_ns = g_quant_delay_ns.load(std::memory_order_relaxed);
+    return iq::launch_gemm_fused_quant(tm_x, tm_w, tm_q, a, fmt, max_pairs, stream) == cudaSuccess ? IQ_OK
+                                                                                                   : IQ_ERR_CUDA;
   }
   return iq::launch_gemm_rope_hadamard_fp4(tm_x, tm_w, tm_q, a, tile_n, fmt, max_pairs, stream) == cudaSuccess
              ? IQ_OK
@@ -202,7 +239,14 @@ iq_status prepare_impl(const void* latent, int M, const void* wq, const uint8_t*
   st = device_setup(&max_pairs);
   if (st != IQ_OK) return st;
   uint8_t* xq = static_cast<uint8_t*>(ws);
-  int32_t* x_sf = reinterpret_cast<int32_t*>(xq + align_up(static_cast<size_t>(M) * iq::kLatentDim, 256));
+  int32_t* x_sf = reinterpret_cast<int32_t*>(xq + prepare_scales_offset(M));
+  // With the fusion switched on, the CTA-pair route quantizes the token rows
+  // inside the GEMM kernel (one launch); otherwise the quantizer runs first.
+  if (g_quant_fusion.load(std::memory_order_relaxed) != 0 && M > g_small_m_max.load(std::memory_order_relaxed) &&
+      gemm_tile_n(M) == 256) {
+    const FusedQuant fuse{latent, reinterpret_cast<unsigned long long*>(xq + prepare_counters_offset(M))};
+    return gemm_stage(xq, x_sf, M, wq, wq_sf, pos, q_fp4, q_sf, q_pre, fmt, max_pairs, stream, &fuse);
+  }
   if (iq::launch_quant_1x128(latent, M, iq::kLatentDim, iq::kLatentDim, xq, iq::kLatentDim, x_sf, stream) !=
       cudaSuccess) {
     return IQ_ERR_CUDA;
@@ -281,7 +325,7 @@ iq_status iq_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t ti
   if (cudaMemsetAsync(workspace, 0, iq_selftest_workspace(), stream) != cudaSuccess) return IQ_ERR_CUDA;
   const int M = 256;
   static const iq::RopeTurns rope = make_rope_turns();
-  iq::GemmArgs a;
+  iq::GemmArgs a{};
   a.x_sf = x_sf;
   a.w_sf = w_sf;
   a.pos = pos;
@@ -293,7 +337,7 @@ iq_status iq_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t ti
   a.num_m_tiles = M / 128;
   a.num_m_pairs = 1;
   a.num_pair_tiles = iq::kQDim / 256;
-  a.token_major = 0;
+  a.order = iq::kOrderFeatureMajor;
   a.timeout_ns = timeout_ns;
   a.rope = rope;
   // The tensor maps are valid descriptors over the workspace (nothing is
@@ -323,7 +367,7 @@ int iq_small_m_threshold(void) { return g_small_m_max.load(); }
 
 void iq_set_gemm_tiling(int tile_n, int order) {
   g_tile_n_override.store(tile_n == 128 || tile_n == 256 ? tile_n : 0);
-  g_order_override.store(order == 1 || order == 2 ? order : 0);
+  g_order_override.store(order >= 1 && order <= 3 ? order : 0);
 }
 
 size_t iq_fp8_scale_words(int M, int K) {
@@ -350,9 +394,12 @@ iq_status iq_fp8_quant_1x128_ue8m0(const void* x_bf16, int M, int K, int ldx, vo
 
 size_t iq_prepare_q_workspace(int M) {
   if (M <= 0) return 0;
-  return align_up(static_cast<size_t>(M) * iq::kLatentDim, 256) +
-         static_cast<size_t>(iq::kScaleGroups) * align_up(static_cast<size_t>(M), 4) * sizeof(int32_t);
+  return prepare_counters_offset(M) + (1 + static_cast<size_t>(iq::kMaxFusedCtas)) * sizeof(unsigned long long);
 }
+
+int iq_set_quant_fusion(int on) { return g_quant_fusion.exchange(on != 0 ? 1 : 0); }
+
+void iq_debug_delay_quant_ns(uint64_t ns) { g_quant_delay_ns.store(ns > kMaxQuantDelayNs ? kMaxQuantDelayNs : ns); }
 
 iq_status iq_prepare_q(const void* latent_bf16, int M, const void* wq_e4m3, const uint8_t* wq_sf,
                        const int32_t* positions, uint8_t* q_fp4, uint8_t* q_sf, void* workspace, size_t ws_bytes,

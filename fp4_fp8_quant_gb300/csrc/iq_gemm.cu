@@ -58,6 +58,7 @@
 #include <cstdint>
 
 #include "iq_fp4.cuh"
+#include "iq_fp8.cuh"
 #include "iq_internal.h"
 #include "iq_ptx.cuh"
 
@@ -120,6 +121,54 @@ struct K2Layout {
 __device__ __forceinline__ void fail(volatile uint32_t* abort_flag, uint32_t bit) {
   atomicOr(&g_iq_status, bit);
   *abort_flag = 1u;
+}
+
+// Progress flags of the fused quantizer, in the caller's workspace: word 0
+// holds the call epoch E, word 1 + c the progress of CTA c as
+// (tag(E, c) << 16) | k, k = the number of waves whose token rows the CTA has
+// written (kExited once all of its threads are done).  Each CTA writes only
+// its own word (plain release stores: no atomics, no contention), and a
+// reader accepts a word only if it carries the tag of this call's epoch and
+// that CTA, a 48-bit hash: a word left by an earlier call (another epoch) or
+// anything a fresh workspace holds matches only by a 2^-48 chance, so no word
+// needs clearing.  CTA 0 finishes last (it waits for every other CTA's exit
+// flag) and then advances the epoch for the next call.
+constexpr uint32_t kExited = 0xFFFFu;
+
+// SplitMix64's finaliser (Steele, Lea and Flood, "Fast splittable
+// pseudorandom number generators") over the epoch and the CTA index.
+__device__ __forceinline__ uint64_t flag_tag(uint64_t epoch, uint32_t cta) {
+  uint64_t z = epoch + 0x9E3779B97F4A7C15ull * (static_cast<uint64_t>(cta) + 1ull);
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return z >> 16;
+}
+
+__device__ __forceinline__ bool flag_reached(uint64_t word, uint64_t tag, uint32_t k) {
+  return (word >> 16) == tag && (word & 0xFFFFull) >= k;
+}
+
+// Wave v of the interleaved order (tiles [vP, vP + P), one per pair) and the
+// rows it reaches first: the 256-row blocks [blk_lo, blk_hi], rows [r0, r1).
+struct WaveRows {
+  int r0, r1;
+  long long units;   // 3 per row: (row, group of four 128-blocks)
+};
+__device__ __forceinline__ WaveRows wave_rows(int v, int P, int T, int M, int tiles_per_row_block) {
+  const int blk_hi = min(v * P + P - 1, T - 1) / tiles_per_row_block;
+  const int blk_lo = v == 0 ? 0 : min(v * P - 1, T - 1) / tiles_per_row_block + 1;
+  WaveRows w;
+  w.r0 = blk_lo * 256;
+  w.r1 = min((blk_hi + 1) * 256, M);
+  w.units = w.r1 > w.r0 ? 3LL * (w.r1 - w.r0) : 0LL;
+  return w;
+}
+
+// The CTA whose contiguous share [U c / G, U (c + 1) / G) of a wave's U units
+// holds unit u.
+__device__ __forceinline__ int unit_owner(long long u, long long units, int G) {
+  return static_cast<int>(((u + 1) * G - 1) / units);
 }
 
 // RoPE, Hadamard, FP4 for one (token, head).  p[j] holds dims (2j, 2j+1) of
@@ -275,10 +324,11 @@ __device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int hea
 // waits all give up with nothing asynchronous in flight (the only tensor-core
 // work is the scale-factor copy, which completes).  It exercises the give-up
 // and teardown path; the product launches only kNoLoads = false.
-template <int kFmt, int kBN, bool kNoLoads = false>
+template <int kFmt, int kBN, bool kNoLoads = false, bool kFuse = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_rope_hadamard_fp4_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ GemmArgs args) {
+  static_assert(!kFuse || (kBN == 256 && !kNoLoads), "the fused quantizer runs with two-head tiles");
   using L = K2Layout<kBN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -335,6 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // Fused quantizer: this call's epoch (CTA 0 advances it only after every
+  // CTA has flagged its exit, so all CTAs read the same value).
+  [[maybe_unused]] uint64_t epoch = 0;
+  if constexpr (kFuse) epoch = *reinterpret_cast<const volatile unsigned long long*>(args.ready);
 
   // Leader-CTA addresses of the barriers that collect the pair's work.
   const uint32_t full_leader0 = mapa_shared(smem_u32(&full[0]), 0);
@@ -342,19 +396,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_empty_leader0 = mapa_shared(smem_u32(&tmem_empty[0]), 0);
 
   // Pair tile pt covers token rows [256 mp, +256) (split by CTA rank) and
-  // features [kBN n, +kBN).  Each pair takes a contiguous run of tiles.  In
-  // feature-major order (mp = pt % num_m_pairs) consecutive tiles share their
-  // heads.  In token-major order (mp = pt / n_tiles, the default) consecutive
-  // tiles share their token rows, so the pairs running at one time read few
-  // distinct X row blocks, each from HBM once, while W (12.6 MB) stays in L2;
-  // measured as fast or faster at every token count.
+  // features [kBN n, +kBN).  In feature-major order (mp = pt % num_m_pairs)
+  // consecutive tiles share their heads; in token-major order (mp = pt /
+  // n_tiles, the default) they share their token rows, so the pairs running
+  // at one time read few distinct X row blocks, each from HBM once, while W
+  // (12.6 MB) stays in L2.  A pair takes a contiguous run of tiles, or, in
+  // the interleaved order, tiles p, p + P, p + 2P, ... (P pairs), so that the
+  // pairs' i-th tiles together form the i-th run of P consecutive tiles.
   constexpr int n_tiles = kQDim / kBN;
   const int num_pairs = static_cast<int>(cluster_count_x());
-  const int tiles_per_pair = (args.num_pair_tiles + num_pairs - 1) / num_pairs;
-  const int first_pt = static_cast<int>(cluster_id_x()) * tiles_per_pair;
-  const int end_pt = min(first_pt + tiles_per_pair, args.num_pair_tiles);
+  const int pair_id = static_cast<int>(cluster_id_x());
+  const bool interleaved = args.order == kOrderInterleaved;
+  int my_first, my_step, my_count;
+  if (interleaved) {
+    my_first = pair_id;
+    my_step = num_pairs;
+    my_count = pair_id < args.num_pair_tiles ? (args.num_pair_tiles - 1 - pair_id) / num_pairs + 1 : 0;
+  } else {
+    const int tiles_per_pair = (args.num_pair_tiles + num_pairs - 1) / num_pairs;
+    my_first = pair_id * tiles_per_pair;
+    my_step = 1;
+    my_count = max(0, min(tiles_per_pair, args.num_pair_tiles - my_first));
+  }
+  auto tile_at = [&](int i) { return my_first + i * my_step; };
   const int num_m_pairs = args.num_m_pairs;
-  const bool token_major = args.token_major != 0;
+  const bool token_major = args.order != kOrderFeatureMajor;
   auto tile_mp = [&](int pt) { return token_major ? pt / n_tiles : pt % num_m_pairs; };
   auto tile_n = [&](int pt) { return token_major ? pt % n_tiles : pt / num_m_pairs; };
   auto tile_m0 = [&](int pt) { return (tile_mp(pt) * kPair + static_cast<int>(rank)) * BM; };
@@ -366,9 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // that kernel.  The stages are fresh, so no release wait precedes them; the
   // leader's expected byte count covers the X loads issued after the wait.
   uint32_t rb[kScaleGroups][L::kHeads];   // producer: the tile's heads' weight-scale words per group
-  auto fetch_w_scales = [&](int pt) {
-    if (pt >= end_pt) return;
-    const int n_tile = tile_n(pt);
+  auto fetch_w_scales = [&](int i) {
+    if (i >= my_count) return;
+    const int n_tile = tile_n(tile_at(i));
 #pragma unroll
     for (int g = 0; g < kScaleGroups; ++g) {
 #pragma unroll
@@ -379,18 +445,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   };
-  const bool have_tile = first_pt < end_pt;
+  const bool have_tile = my_count > 0;
   if (warp == 0) {
     if constexpr (!kNoLoads) {
       if (lane == 0 && have_tile) {
-        const int n0 = tile_n(first_pt) * kBN + static_cast<int>(rank) * (kBN / kPair);
+        const int n0 = tile_n(tile_at(0)) * kBN + static_cast<int>(rank) * (kBN / kPair);
         for (int kb = 0; kb < kStages; ++kb) {
           if (leader) mbar_arrive_expect_tx(&full[kb], L::kStageTx);
           tma_load_2d_pair(sB + kb * L::kBBytes, &tm_w, full_leader0 + 8u * kb, kb * BK, n0);
         }
       }
     }
-    fetch_w_scales(first_pt);
+    fetch_w_scales(0);
   }
   // Launched with programmatic stream serialization: everything above
   // overlapped the preceding kernel; nothing below runs before it completed
@@ -402,11 +468,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0;
     uint32_t issued_mask = 0, issued_phase = 0;   // per stage: a load was issued / its phase
+    // Fused quantizer: before it reads a tile's token rows (FP8 codes by TMA,
+    // scale words by plain loads) the producer waits until the block's
+    // counter shows all of its units written (3 per row), acquires it, and
+    // orders the async proxy behind it.  All lanes take part.
+    auto rows_ready = [&](int i) -> bool {
+      if constexpr (!kFuse) {
+        return true;
+      } else {
+        if (i >= my_count) return true;
+        const int pt = tile_at(i);
+        const int m0 = tile_m0(pt);
+        const int rows = min(BM, args.M - m0);
+        if (rows <= 0) return true;   // rows past M: the loads read zeros
+        // The wave that first reaches this row block, and the CTAs whose
+        // shares of that wave hold the block's units.
+        const int v = (tile_mp(pt) * n_tiles) / num_pairs;
+        const WaveRows w = wave_rows(v, num_pairs, args.num_pair_tiles, args.M, n_tiles);
+        const long long u0 = 3LL * (m0 - w.r0), u1 = u0 + 3LL * rows;
+        const int G = static_cast<int>(gridDim.x);
+        const int c_lo = unit_owner(u0, w.units, G), c_hi = unit_owner(u1 - 1, w.units, G);
+        const uint32_t need = static_cast<uint32_t>(v + 1);
+        bool ok = true;
+        for (int c = c_lo + lane; c <= c_hi && ok; c += 32) {
+          const uint64_t tag = flag_tag(epoch, static_cast<uint32_t>(c));
+          const unsigned long long* f = args.ready + 1 + c;
+          if (!flag_reached(ld_acquire_u64(f), tag, need)) {
+            const uint64_t t0 = globaltimer_ns();
+            while (true) {
+              __nanosleep(32);
+              if (flag_reached(ld_acquire_u64(f), tag, need)) break;
+              if (globaltimer_ns() - t0 > timeout) {
+                ok = false;
+                break;
+              }
+            }
+          }
+        }
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (ok) fence_proxy_async_global();
+        return ok;
+      }
+    };
+    if constexpr (kFuse) {
+      // The first tile's X loads go out whatever the outcome, so that every
+      // stage whose W half is in flight completes.
+      if (have_tile && !rows_ready(0) && lane == 0) fail(abort_flag, kStatusRowsWait);
+    }
     // The first tile's X loads of the first pass go out at once (their W
     // halves are already in flight), ahead of the scale-word reads.
     if constexpr (!kNoLoads) {
       if (lane == 0 && have_tile) {
-        const int m0 = tile_m0(first_pt);
+        const int m0 = tile_m0(tile_at(0));
         for (int kb = 0; kb < kStages; ++kb)
           tma_load_2d_pair(sA + kb * kABytes, &tm_x, full_leader0 + 8u * kb, kb * BK, m0);
         issued_mask = (1u << kStages) - 1u;
@@ -419,9 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile boundary.  ra: this lane's 4 rows x 3 groups of activation-scale
     // words (written by the preceding kernel: read after the wait).
     uint32_t ra[kScaleGroups][4];
-    auto fetch_x_scales = [&](int pt) {
-      if (pt >= end_pt) return;
-      const int m0 = tile_m0(pt);
+    auto fetch_x_scales = [&](int i) {
+      if (i >= my_count) return;
+      const int m0 = tile_m0(tile_at(i));
 #pragma unroll
       for (int g = 0; g < kScaleGroups; ++g) {
 #pragma unroll
@@ -431,12 +544,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    fetch_x_scales(first_pt);
-    int local = 0;
-    for (int pt = first_pt; pt < end_pt; ++pt, ++local) {
+    fetch_x_scales(0);
+    for (int local = 0; local < my_count; ++local) {
       // Every exit decision is made warp-uniform: the lanes must stay
       // converged for the shuffles below.
       if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
+      const int pt = tile_at(local);
       const int m0 = tile_m0(pt);
       const int n_tile = tile_n(pt);
       const int buf = local & 1;
@@ -459,8 +572,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      fetch_x_scales(pt + 1);
-      fetch_w_scales(pt + 1);
+      if constexpr (!kFuse) {
+        fetch_x_scales(local + 1);
+        fetch_w_scales(local + 1);
+      }
       bool ok = true;
       if (lane == 0) {
         mbar_arrive_cluster(sf_full_leader0 + 8u * static_cast<uint32_t>(buf));
@@ -487,6 +602,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
+      if constexpr (kFuse) {
+        // After this tile's loads, so that a wait for the next tile's rows
+        // never holds them back; the scale reads overlap the tile's last
+        // MMAs.
+        fetch_w_scales(local + 1);
+        if (!rows_ready(local + 1)) {
+          if (lane == 0) fail(abort_flag, kStatusRowsWait);
+          break;
+        }
+        fetch_x_scales(local + 1);
+      }
     }
     // Teardown: this CTA's loads signal the leader's barriers, so their
     // landing is observed through the stage's release by the pair's MMAs,
@@ -504,12 +630,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------- MMA issuer (leader)
     if (lane == 0) {
       if (leader) {
-        int local = 0;
         bool ok = true;
         const uint64_t adesc0 = smem_desc_sw128(smem_u32(sA));
         const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sB));
         const uint32_t idesc0 = idesc_mxf8_e4m3(kPair * BM, kBN, 0, 0);
-        for (int pt = first_pt; pt < end_pt && ok; ++pt, ++local) {
+        for (int local = 0; local < my_count && ok; ++local) {
           if (*abort_flag) break;
           const int buf = local & 1;
           const int acc = local % L::kAccBufs;
@@ -594,8 +719,100 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stage_row = sOut + half * kOutHeadBytes + trow * 64;
     const int swz = (trow >> 1) & 3;
     const bool store_issuer = warp == 2 && lane == 0;
-    int local = 0;
-    for (int pt = first_pt; pt < end_pt; ++pt, ++local) {
+    // Fused quantizer.  Wave v of the interleaved order is the run of tiles
+    // [vP, vP + P), one per pair, and a pair's i-th tile lies in wave i.  The
+    // wave's new rows are the 256-row blocks that no earlier wave reaches;
+    // their units (row, group of four 128-blocks) are split into G equal
+    // contiguous ranges, one per CTA, and dealt round-robin to its eight
+    // epilogue warps.  A producer needs wave i + 1's rows when its MMAs are
+    // half way through tile i (the ring runs half a tile ahead), so the warps
+    // quantize waves 0, 1 and 2 before the first accumulator wait and wave
+    // i + 2 before the wait for tile i, after tile i - 1's epilogue: at least
+    // half a tile of slack.  After its share of a wave the CTA publishes the
+    // number of waves it has done in its progress flag.
+    [[maybe_unused]] int q_next = 0;
+    [[maybe_unused]] const int num_waves = (args.num_pair_tiles + num_pairs - 1) / num_pairs;
+    auto quantize_wave = [&](int v) {
+      const WaveRows w = wave_rows(v, num_pairs, args.num_pair_tiles, args.M, n_tiles);
+      const int r0 = w.r0;
+      const long long units = w.units;
+      const long long G = gridDim.x;
+      const long long lo = units * blockIdx.x / G, hi = units * (blockIdx.x + 1) / G;
+      const int ew = warp - 2;
+      auto unit_src = [&](long long u) {
+        return args.latent + static_cast<long long>(r0 + static_cast<int>(u / 3)) * kLatentDim +
+               static_cast<int>(u % 3) * 512 + lane * 16;
+      };
+      auto unit_store = [&](long long u, const uint4& a, const uint4& b) {
+        const int row = r0 + static_cast<int>(u / 3);
+        const int g = static_cast<int>(u % 3);
+        uint4 codes;
+        const uint32_t word = fp8_quant_unit(a, b, true, codes);
+        *reinterpret_cast<uint4*>(args.x_fp8 + static_cast<long long>(row) * kLatentDim + g * 512 + lane * 16) = codes;
+        if (lane == 0) {
+          int32_t* sf = args.x_sf_out + static_cast<long long>(g) * args.m_al;
+          sf[row] = static_cast<int32_t>(word);
+          if (row == args.M - 1)
+            for (int r = args.M; r < args.m_al; ++r) sf[r] = 0;   // pad rows, as the quantizer kernel writes them
+        }
+      };
+      // Two units per warp in flight: both loads go out before either unit
+      // is reduced.
+      for (long long u = lo + ew; u < hi; u += 2 * kNumEpiWarps) {
+        const long long u2 = u + kNumEpiWarps;
+        const bool two = u2 < hi;   // warp-uniform
+        const uint16_t* s1 = unit_src(u);
+        const uint4 a1 = ld_stream_v4(s1), b1 = ld_stream_v4(s1 + 8);
+        uint4 a2 = make_uint4(0, 0, 0, 0), b2 = a2;
+        if (two) {
+          const uint16_t* s2 = unit_src(u2);
+          a2 = ld_stream_v4(s2);
+          b2 = ld_stream_v4(s2 + 8);
+        }
+        unit_store(u, a1, b1);
+        if (two) unit_store(u2, a2, b2);
+      }
+      if (args.quant_delay_ns != 0ull && lane == 0) {
+        // Diagnostics only: holds back the wave's signal (bounded by the delay).
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < args.quant_delay_ns) {
+        }
+      }
+      // The warps meet, then one thread publishes the CTA's progress with a
+      // release (cumulative over the other threads' stores, which the
+      // barrier ordered before it).
+      named_barrier_sync(1, kNumEpiWarps * 32);
+      if (ew == 0 && lane == 0) {
+        __threadfence();
+        st_release_u64(args.ready + 1 + blockIdx.x,
+                       (flag_tag(epoch, blockIdx.x) << 16) | static_cast<uint64_t>(v + 1));
+      }
+    };
+    // One tile ahead of its quantization, the CTA's share of a wave's token
+    // rows is fetched from HBM into L2 (asynchronous bulk prefetches, one per
+    // 1 KB unit), so that the warps' loads later hit L2.
+    auto prefetch_wave = [&](int v) {
+      if constexpr (kFuse) {
+        if (v >= num_waves) return;
+        const WaveRows w = wave_rows(v, num_pairs, args.num_pair_tiles, args.M, n_tiles);
+        const long long G = gridDim.x;
+        const long long lo = w.units * blockIdx.x / G, hi = w.units * (blockIdx.x + 1) / G;
+        for (long long u = lo + (warp - 2) * 32 + lane; u < hi; u += kNumEpiWarps * 32) {
+          const uint16_t* src = args.latent + static_cast<long long>(w.r0 + static_cast<int>(u / 3)) * kLatentDim +
+                                static_cast<int>(u % 3) * 512;
+          prefetch_l2_bulk(src, 1024);
+        }
+      }
+    };
+    auto quantize_through = [&](int v_last) {
+      if constexpr (kFuse) {
+        for (; q_next <= v_last && q_next < num_waves; ++q_next) quantize_wave(q_next);
+        prefetch_wave(q_next);
+      }
+    };
+    for (int local = 0; local < my_count; ++local) {
+      quantize_through(local + 2);
+      const int pt = tile_at(local);
       const int row = tile_m0(pt) + trow;
       const int head = tile_n(pt) * L::kHeads + half;
       const int acc = local % L::kAccBufs;
@@ -645,6 +862,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_store_commit();
       }
     }
+    // A pair with fewer tiles than waves still owes its share of the rest.
+    quantize_through(num_waves - 1);
     // The staging tile must stay valid until the last bulk stores have read
     // it; their writes to global memory complete with the grid.
     if (store_issuer) tma_store_wait_read();
@@ -657,6 +876,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc_pair(tmem, kTmemCols);
+  }
+  if constexpr (kFuse) {
+    // Every CTA flags its exit once all of its threads are done.  CTA 0 then
+    // waits (bounded) for all the others, so that no CTA of this call can
+    // still read the epoch, and advances it for the next call (also when the
+    // wait gives up, so that a later call never meets this call's flags).
+    if (threadIdx.x == 0) {
+      __threadfence();
+      st_release_u64(args.ready + 1 + blockIdx.x, (flag_tag(epoch, blockIdx.x) << 16) | kExited);
+    }
+    if (blockIdx.x == 0 && warp == 0) {
+      // The 32 lanes poll the other CTAs' flags side by side.
+      const uint64_t t0 = globaltimer_ns();
+      bool ok = true;
+      for (uint32_t c = 1 + lane; c < gridDim.x && ok; c += 32) {
+        const uint64_t tag = flag_tag(epoch, c);
+        while (!flag_reached(ld_acquire_u64(args.ready + 1 + c), tag, kExited)) {
+          if (globaltimer_ns() - t0 > 2 * timeout) {
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (lane == 0) {
+        if (!ok) atomicOr(&g_iq_status, kStatusRowsWait);
+        *reinterpret_cast<volatile unsigned long long*>(args.ready) = epoch + 1ull;
+      }
+    }
   }
 }
 
@@ -681,10 +930,34 @@ cudaLaunchConfig_t pair_config(int pairs, int smem_bytes, cudaLaunchAttribute* a
   return cfg;
 }
 
-template <int kFmt, int kBN, bool kNoLoads = false>
+template <int kFmt, int kBN, bool kNoLoads = false, bool kFuse = false>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_rope_hadamard_fp4_kernel<kFmt, kBN, kNoLoads>,
+  return cudaFuncSetAttribute(gemm_rope_hadamard_fp4_kernel<kFmt, kBN, kNoLoads, kFuse>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, K2Layout<kBN>::kSmemBytes);
+}
+
+// The fused-quantizer instance: clusters of two, launched cooperatively so
+// that all CTAs are resident together (each waits for token rows that CTAs
+// all over the grid quantize), and without programmatic serialization (it
+// reads its inputs before any dependency wait).
+template <int kFmt>
+cudaError_t launch_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
+                         const GemmArgs& args, int pairs, cudaStream_t stream) {
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pairs * kPair, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = K2Layout<256>::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_rope_hadamard_fp4_kernel<kFmt, 256, false, true>, tm_x, tm_w, tm_q, args);
 }
 
 template <int kFmt, int kBN, bool kNoLoads = false>
@@ -710,7 +983,8 @@ int gemm_pair_size() { return kPair; }
 cudaError_t gemm_setup_device(int* max_pairs) {
   for (cudaError_t err : {set_smem_attr<kFp4Mx, 256>(), set_smem_attr<kFp4MxOcp, 256>(), set_smem_attr<kFp4Nv, 256>(),
                           set_smem_attr<kFp4Mx, 128>(), set_smem_attr<kFp4MxOcp, 128>(), set_smem_attr<kFp4Nv, 128>(),
-                          set_smem_attr<kFp4Mx, 256, true>()}) {
+                          set_smem_attr<kFp4Mx, 256, true>(), set_smem_attr<kFp4Mx, 256, false, true>(),
+                          set_smem_attr<kFp4MxOcp, 256, false, true>(), set_smem_attr<kFp4Nv, 256, false, true>()}) {
     if (err != cudaSuccess) return err;
   }
   // One CTA per SM for either width (tensor memory and registers), so the
@@ -737,6 +1011,22 @@ cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtenso
     case kFp4Mx: return launch_one<kFp4Mx, 256>(tm_x, tm_w, tm_q, args, pairs, stream);
     case kFp4MxOcp: return launch_one<kFp4MxOcp, 256>(tm_x, tm_w, tm_q, args, pairs, stream);
     case kFp4Nv: return launch_one<kFp4Nv, 256>(tm_x, tm_w, tm_q, args, pairs, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_gemm_fused_quant(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
+                                    const GemmArgs& args, int fp4_format, int max_pairs, cudaStream_t stream) {
+  if (args.order != kOrderInterleaved || args.latent == nullptr || args.x_fp8 == nullptr ||
+      args.x_sf_out == nullptr || args.ready == nullptr) {
+    return cudaErrorInvalidValue;
+  }
+  const int pairs = launch_pairs(args.num_pair_tiles, max_pairs);
+  if (pairs * kPair > kMaxFusedCtas) return cudaErrorInvalidValue;
+  switch (fp4_format) {
+    case kFp4Mx: return launch_fused<kFp4Mx>(tm_x, tm_w, tm_q, args, pairs, stream);
+    case kFp4MxOcp: return launch_fused<kFp4MxOcp>(tm_x, tm_w, tm_q, args, pairs, stream);
+    case kFp4Nv: return launch_fused<kFp4Nv>(tm_x, tm_w, tm_q, args, pairs, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -44,6 +44,14 @@ struct RopeTurns {
   float lo[32];
 };
 
+// Most CTAs a fused-quantizer launch may have (progress flags in the workspace).
+constexpr int kMaxFusedCtas = 512;
+
+// Pair-tile orders of the CTA-pair kernel (GemmArgs::order).
+constexpr int kOrderFeatureMajor = 0;   // contiguous runs, consecutive tiles share heads
+constexpr int kOrderTokenMajor = 1;     // contiguous runs, consecutive tiles share token rows
+constexpr int kOrderInterleaved = 2;    // token-major tiles dealt round-robin to the pairs
+
 struct GemmArgs {
   const int32_t* x_sf;   // [3][m_al] packed UE8M0 words of the FP8 latent
   const uint8_t* w_sf;   // [64][12] UE8M0 bytes of the weight blocks
@@ -56,9 +64,17 @@ struct GemmArgs {
   int num_m_tiles;
   int num_m_pairs;       // ceil(num_m_tiles / 2): 256-token row blocks of a CTA pair
   int num_pair_tiles;    // num_m_pairs * (8192 / tile width) pair tiles
-  int token_major;       // pair-tile order: 0 feature-major, 1 token-major
+  int order;             // pair-tile order: kOrderFeatureMajor, kOrderTokenMajor, kOrderInterleaved
   unsigned long long timeout_ns;
   RopeTurns rope;
+  // The quantizer fused into the CTA-pair kernel (interleaved order only):
+  // the kernel itself writes the FP8 rows and scale words that it reads
+  // through tm_x and x_sf, and counts finished work per 128-row block.
+  const uint16_t* latent;        // [M][1536] BF16 bits
+  uint8_t* x_fp8;                // [M][1536] E4M3 codes (tm_x's memory)
+  int32_t* x_sf_out;             // [3][m_al] packed words (x_sf's memory)
+  unsigned long long* ready;     // [1 + kMaxFusedCtas] epoch and per-CTA progress flags, see iq_gemm.cu
+  unsigned long long quant_delay_ns;   // diagnostics: delay before each wave's signal
 };
 
 // Status bits of the device status word (which wait gave up).
@@ -67,6 +83,7 @@ enum : uint32_t {
   kStatusMmaWait = 1u << 1,
   kStatusEpilogueWait = 1u << 2,
   kStatusTeardownWait = 1u << 3,
+  kStatusRowsWait = 1u << 4,     // fused quantizer: token rows not ready in time
 };
 
 cudaError_t launch_quant_1x128(const void* x, int M, int K, long long ldx, void* y, long long ldy, int32_t* sf,
@@ -92,6 +109,12 @@ int gemm_pair_size();
 cudaError_t launch_gemm_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
                                           const GemmArgs& args, int tile_n, int fp4_format, int max_pairs,
                                           cudaStream_t stream);
+
+// The same kernel with the quantizer fused in (two-head tiles, interleaved
+// order; args.latent, x_fp8, x_sf_out and ready set): one launch for the whole
+// preparation.  All CTAs run at once (a cooperative launch).
+cudaError_t launch_gemm_fused_quant(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const CUtensorMap& tm_q,
+                                    const GemmArgs& args, int fp4_format, int max_pairs, cudaStream_t stream);
 
 // The fused GEMM kernel's wait self-test instance (no TMA loads: every wait
 // that depends on them gives up after args.timeout_ns).

@@ -151,6 +151,33 @@ __device__ __forceinline__ uint32_t ld_dependent_u32(const void* p) {
   return v;
 }
 
+// 64-bit load with acquire semantics at GPU scope: later memory accesses of
+// this thread see what the releasing writer wrote before its release.
+__device__ __forceinline__ uint64_t ld_acquire_u64(const void* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(reinterpret_cast<uint64_t>(p)) : "memory");
+  return v;
+}
+
+// Asynchronous prefetch of `bytes` (a multiple of 16, 16-byte aligned) of
+// global memory into L2; nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
+// 64-bit store with release semantics at GPU scope.
+__device__ __forceinline__ void st_release_u64(void* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "l"(v) : "memory");
+}
+
+// Orders generic-proxy accesses to global memory against later async-proxy
+// accesses (TMA) of this thread: data acquired through a flag becomes
+// visible to the bulk tensor loads issued after it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Lets the dependent grid of the stream be scheduled before this one ends.
 __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -48,14 +48,6 @@ constexpr int kThreads = 256;
 // blocks are spread; one block per SM keeps ~0.6 MB of loads in flight.
 constexpr int kHostThreads = 128;
 
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
 __global__ void __launch_bounds__(kThreads) quant_1x128_kernel(const uint16_t* __restrict__ x, int M, int K,
                                                                long long ldx, uint8_t* __restrict__ y,
                                                                long long ldy, int32_t* __restrict__ sf, int m_al,
@@ -74,39 +66,13 @@ __global__ void __launch_bounds__(kThreads) quant_1x128_kernel(const uint16_t* _
   uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
   const uint16_t* src = x + row * ldx + col;
   if (active) {
-    a = ld_stream(src);
-    b = ld_stream(src + 8);
+    a = ld_stream_v4(src);
+    b = ld_stream_v4(src + 8);
   }
-  uint32_t m2 = abs_max_bf16x2(0u, a.x);
-  m2 = abs_max_bf16x2(m2, a.y);
-  m2 = abs_max_bf16x2(m2, a.z);
-  m2 = abs_max_bf16x2(m2, a.w);
-  m2 = abs_max_bf16x2(m2, b.x);
-  m2 = abs_max_bf16x2(m2, b.y);
-  m2 = abs_max_bf16x2(m2, b.z);
-  m2 = abs_max_bf16x2(m2, b.w);
-  uint32_t m1 = max(m2 & 0xFFFFu, m2 >> 16);
-  m1 = max(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, 1));
-  m1 = max(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, 2));
-  m1 = max(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, 4));
-  const float amax = __uint_as_float(m1 << 16);
-
-  const int e = fp8_scale_exponent(amax);
-  const float inv = fp8_inv_scale(e);
-  if (active) {
-    uint4 out;
-    out.x = quant_quad(a.x, a.y, inv);
-    out.y = quant_quad(a.z, a.w, inv);
-    out.z = quant_quad(b.x, b.y, inv);
-    out.w = quant_quad(b.z, b.w, inv);
-    *reinterpret_cast<uint4*>(y + row * ldy + col) = out;
-  }
-  const uint32_t byte = active ? static_cast<uint32_t>(e + 127) : 0u;
-  const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, byte, 0);
-  const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, byte, 8);
-  const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, byte, 16);
-  const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, byte, 24);
-  if (lane == 0) sf[static_cast<long long>(g) * m_al + row] = static_cast<int32_t>(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24));
+  uint4 out;
+  const uint32_t word = fp8_quant_unit(a, b, active, out);
+  if (active) *reinterpret_cast<uint4*>(y + row * ldy + col) = out;
+  if (lane == 0) sf[static_cast<long long>(g) * m_al + row] = static_cast<int32_t>(word);
 }
 
 __global__ void __launch_bounds__(kHostThreads)
@@ -136,8 +102,8 @@ __global__ void __launch_bounds__(kHostThreads)
 
     uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
     const uint16_t* src = x + row * ldx;
-    if (active_a) a = ld_stream(src + col_a);
-    if (active_b) b = ld_stream(src + col_b);
+    if (active_a) a = ld_stream_v4(src + col_a);
+    if (active_b) b = ld_stream_v4(src + col_b);
     uint32_t ma = abs_max_bf16x2(0u, a.x);
     ma = abs_max_bf16x2(ma, a.y);
     ma = abs_max_bf16x2(ma, a.z);

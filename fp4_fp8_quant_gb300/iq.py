@@ -45,6 +45,8 @@ SIGNATURES = {
     "iq_set_small_m_threshold": (_I, [_I]),
     "iq_small_m_threshold": (_I, []),
     "iq_set_gemm_tiling": (None, [_I, _I]),
+    "iq_set_quant_fusion": (_I, [_I]),
+    "iq_debug_delay_quant_ns": (None, [ctypes.c_uint64]),
     "iq_fp4_scale_bytes": (_SZ, [_I]),
     "iq_prepare_q_ex": (_I, [_P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
     "iq_prepare_q_host_workspace": (_SZ, [_I, _I]),
@@ -292,9 +294,20 @@ def device_status(reset: bool = False) -> int:
 
 def set_gemm_tiling(tile_n: int = 0, order: int = 0) -> None:
     """Tuning override of the CTA-pair kernel's tiling (include/iq.h,
-    iq_set_gemm_tiling): tile_n 128 or 256, order 1 feature-major or 2
-    token-major; 0 restores the default."""
+    iq_set_gemm_tiling): tile_n 128 or 256, order 1 feature-major, 2
+    token-major or 3 interleaved; 0 restores the default."""
     lib().iq_set_gemm_tiling(int(tile_n), int(order))
+
+
+def set_quant_fusion(on: bool) -> bool:
+    """The quantizer fused into the CTA-pair kernel (include/iq.h,
+    iq_set_quant_fusion); returns the previous setting."""
+    return bool(lib().iq_set_quant_fusion(1 if on else 0))
+
+
+def debug_delay_quant_ns(ns: int) -> None:
+    """Diagnostics: delay of the fused quantizer's signals (iq_debug_delay_quant_ns)."""
+    lib().iq_debug_delay_quant_ns(int(ns))
 
 
 def set_wait_timeout_ns(ns: int) -> None:

@@ -132,10 +132,25 @@ int iq_small_m_threshold(void);
  * their 256 token rows).  tile_n: 128 (one head per tile, two accumulators
  * in tensor memory) or 256 forces that width, any other value restores the
  * default; order: 1 forces feature-major (consecutive tiles share their
- * heads), 2 token-major, any other value restores the default.
+ * heads), 2 token-major, 3 interleaved (token-major tiles dealt round-robin
+ * to the pairs: pair p takes tiles p, p + P, ...), any other value restores
+ * the default.
  * Results are the same under every setting (the same sums in the same order
  * per output).  Process-wide; applies to later calls. */
 void iq_set_gemm_tiling(int tile_n, int order);
+
+/* The quantizer fused into the CTA-pair kernel: off (0, the default: the
+ * stand-alone quantizer, then the GEMM kernel) or on (1: one launch, see
+ * iq_prepare_q).  Results are the same either way; on GB300 the fused launch
+ * measured slower at every token count, so it is off unless asked for.  The
+ * fusion also needs two-head tiles (see iq_set_gemm_tiling).  Process-wide;
+ * applies to later calls; returns the previous setting. */
+int iq_set_quant_fusion(int on);
+
+/* Diagnostics: the fused quantizer's warps wait ns nanoseconds (at most 1 ms)
+ * before signalling each wave of token rows, so that the GEMM's loads must
+ * wait for them.  0 (the default) turns it off.  Process-wide. */
+void iq_debug_delay_quant_ns(uint64_t ns);
 
 /* ------------------------------------------------------------------------
  * 1. FP8 1x128 quantizer with packed UE8M0 scales.
@@ -187,7 +202,11 @@ iq_status iq_fp8_quant_1x128_ue8m0(const void* x_bf16, int M, int K, int ldx,
 
 /* Workspace bytes iq_prepare_q needs for M tokens: the E4M3 latent
  * [M, 1536] at offset 0 followed, at the next 256-byte boundary, by its packed
- * scale words [3][align_up(M, 4)].  Returns 0 when M <= 0. */
+ * scale words [3][align_up(M, 4)], then, at the next 256-byte boundary, the
+ * fused quantizer's flags (513 words of 8 bytes: a call counter and one
+ * progress word per CTA).  The flags need no initialisation: a progress word
+ * counts only if it carries a 48-bit hash of the current call counter and its
+ * CTA, which each call advances.  Returns 0 when M <= 0. */
 size_t iq_prepare_q_workspace(int M);
 
 /* Arguments:
@@ -205,19 +224,27 @@ size_t iq_prepare_q_workspace(int M);
  *   workspace    caller scratch of at least iq_prepare_q_workspace(M) bytes,
  *                256-byte aligned; its contents on return are the FP8 latent
  *                and its packed scales (operation 1's outputs).
- * M == 0 returns IQ_OK without a launch.  Two kernel launches, back to back
- * on `stream`: the quantizer, then the fused GEMM kernel of M's route (see
- * iq_set_small_m_threshold), launched as the quantizer's programmatic
- * dependent so that its set-up (and, on the small-M route, its weight loads)
- * overlap the quantizer.
+ * M == 0 returns IQ_OK without a launch.
  *
- * Ordering: the GEMM kernel of the small-M route reads wq_e4m3 and wq_sf
- * before the kernel launched just before it on `stream` has completed (that
- * kernel is the quantizer for iq_prepare_q; for iq_gemm_rope_hadamard_fp4 it
- * is whatever the caller launched last, and the overlap happens only if that
- * kernel allows programmatic dependents).  The weights must therefore not be
- * written by the immediately preceding kernel.  Every other input is read
- * after that kernel has completed. */
+ * Launches.  Two kernel launches, back to back on `stream`: the quantizer,
+ * then the GEMM kernel of M's route (see iq_set_small_m_threshold), launched
+ * as the quantizer's programmatic dependent so that its set-up (and, on the
+ * small-M route, its weight loads) overlap the quantizer.  With the fusion
+ * switched on (iq_set_quant_fusion) the CTA-pair route is ONE launch: the
+ * GEMM kernel quantizes the token rows itself (operation 1's arithmetic, the
+ * same codes and scale words in the workspace) in waves ahead of the tiles
+ * that read them, and a tile's loads wait for the progress flags of the CTAs
+ * that quantized its rows; that launch is cooperative (all of its CTAs, one
+ * per SM, resident at once).
+ *
+ * Ordering: the small-M GEMM kernel reads wq_e4m3 and wq_sf before the kernel
+ * launched just before it on `stream` has completed (that kernel is the
+ * quantizer for iq_prepare_q; for iq_gemm_rope_hadamard_fp4 it is whatever
+ * the caller launched last, and the overlap happens only if that kernel
+ * allows programmatic dependents).  The weights must therefore not be written
+ * by the immediately preceding kernel.  Every other input is read after that
+ * kernel has completed.  Calls that run at the same time must not share a
+ * workspace. */
 iq_status iq_prepare_q(const void* latent_bf16, int M,
                        const void* wq_e4m3, const uint8_t* wq_sf,
                        const int32_t* positions,

@@ -45,8 +45,11 @@ def test_size_helpers(lib):
     assert lib.iq_fp8_scale_words(5, 1536) == 3 * 8
     assert lib.iq_fp8_scale_words(5, 640) == 2 * 8
     assert lib.iq_fp8_scale_words(0, 1536) == 0
-    assert lib.iq_prepare_q_workspace(4632) == 4632 * 1536 + 3 * 4632 * 4
-    assert lib.iq_prepare_q_workspace(5) == 7680 + 3 * 8 * 4
+    # FP8 latent, scale words at the next 256-byte boundary, then the fused
+    # quantizer's flags (an epoch word and 512 progress words) at the next one
+    assert lib.iq_prepare_q_workspace(4632) == 7170560 + 513 * 8
+    assert (4632 * 1536 + 3 * 4632 * 4 + 255) // 256 * 256 == 7170560
+    assert lib.iq_prepare_q_workspace(5) == (7680 + 3 * 8 * 4 + 255) // 256 * 256 + 513 * 8
     assert lib.iq_prepare_q_workspace(0) == 0
 
 
@@ -137,3 +140,14 @@ def test_host_entry_sizes_settings_and_checks(lib):
     assert lib.iq_prepare_q_host(16, 4, 16, 16, 16, 0, 16, 16, 256, need - 1, None) == -6
     assert lib.iq_prepare_q_host(24, 4, 16, 16, 16, 0, 16, 16, 256, need, None) == -2    # latent alignment
 
+
+
+def test_quant_fusion_switch_is_host_state(lib):
+    old = lib.iq_set_quant_fusion(0)
+    try:
+        assert old == 0, "off by default"
+        assert lib.iq_set_quant_fusion(5) == 0
+        assert lib.iq_set_quant_fusion(0) == 1
+        assert lib.iq_set_quant_fusion(1) == 0
+    finally:
+        lib.iq_set_quant_fusion(old)

@@ -1,9 +1,10 @@
-"""Topology of a captured iq_prepare_q call: exactly two kernel nodes (the
-quantizer and the fused GEMM of the call's route) and nothing else -- no
-separate RoPE, Hadamard or FP4 kernel, no memcpy and no memset node.  This is
-the check the TensorRT-LLM PR "Fuse DeepSeek-V4 Indexer Q projection with CuTe
-DSL" makes on its fused path (Description: no standalone RoPE or FP4-concat
-kernel in the captured graph).
+"""Topology of a captured iq_prepare_q call: kernel nodes only -- no
+separate RoPE, Hadamard or FP4 kernel, no memcpy and no memset node.  The
+quantizer and the GEMM kernel of the call's route are two kernel nodes; with
+the quantizer fused into the CTA-pair kernel (iq_set_quant_fusion) that route
+is one.  This is the check the TensorRT-LLM PR "Fuse DeepSeek-V4 Indexer
+Q projection with CuTe DSL" makes on its fused path (Description: no
+standalone RoPE or FP4-concat kernel in the captured graph).
 
 The graph is captured on a torch stream with the driver API (libcuda through
 ctypes) so that its nodes can be listed.
@@ -59,9 +60,18 @@ def _node_types(call, stream):
         cu.cuGraphDestroy(graph)
 
 
-@pytest.mark.parametrize("M", [24, 300, 4632])
-def test_captured_prepare_q_is_two_kernels(cuda_device, M):
+@pytest.mark.parametrize("M,fused,kernels", [(24, True, 2), (300, True, 1), (4632, True, 1),
+                                              (300, False, 2), (4632, False, 2)])
+def test_captured_prepare_q_kernel_nodes(cuda_device, M, fused, kernels):
     from fp4_fp8_quant_gb300 import iq
+    prev = iq.set_quant_fusion(fused)
+    try:
+        _check_topology(iq, M, kernels)
+    finally:
+        iq.set_quant_fusion(prev)
+
+
+def _check_topology(iq, M, kernels):
     x, wq, wsf, pos = W.chain_workload(M, seed=600 + M, outlier_p=0.001, outlier_scale=50.0)
     lat = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda()
     w, ws, p = torch.from_numpy(wq).cuda(), torch.from_numpy(wsf).cuda(), torch.from_numpy(pos).cuda()
@@ -72,4 +82,4 @@ def test_captured_prepare_q_is_two_kernels(cuda_device, M):
     torch.cuda.synchronize()
     stream = torch.cuda.Stream()
     types = _node_types(lambda: iq.prepare_q(lat, w, ws, p, q_fp4=q, q_sf=s, workspace=work, stream=stream), stream)
-    assert types == [CU_GRAPH_NODE_TYPE_KERNEL] * 2, types
+    assert types == [CU_GRAPH_NODE_TYPE_KERNEL] * kernels, types

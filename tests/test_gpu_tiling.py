@@ -1,8 +1,10 @@
 """The CTA-pair kernel's tilings: one head (128 features) or two heads (256)
-per pair tile, feature-major or token-major tile order.  Every setting
-computes each output with the same sums in the same order, so all of them must
-give the same bytes, and the default route (two heads per tile, token-major
-order) must match the oracle at the mid-size token counts."""
+per pair tile; feature-major, token-major or interleaved tile order.  Every
+setting computes each output with the same sums in the same order, so all of
+them must give the same bytes, and the default route must match the oracle at
+the mid-size token counts.  The tilings are exercised with the quantizer as a
+separate launch (the fused route always takes two-head tiles in the
+interleaved order)."""
 
 import contextlib
 
@@ -26,10 +28,12 @@ def _iq():
 def _tiling(tile_n, order):
     iq = _iq()
     iq.set_gemm_tiling(tile_n, order)
+    prev = iq.set_quant_fusion(False)
     try:
         yield
     finally:
         iq.set_gemm_tiling(0, 0)
+        iq.set_quant_fusion(prev)
 
 
 def _dev(x, pos, wq, wsf):
@@ -57,7 +61,7 @@ def test_every_tiling_gives_the_same_bytes(cuda_device, M, fmt):
     lat, w, ws, p = _dev(x, pos, wq, wsf)
     outs = {}
     for tile_n in (128, 256):
-        for order in (1, 2):
+        for order in (1, 2, 3):
             with _tiling(tile_n, order):
                 outs[(tile_n, order)] = iq.prepare_q(lat, w, ws, p, debug=True, fp4_format=fmt)
     torch.cuda.synchronize()
