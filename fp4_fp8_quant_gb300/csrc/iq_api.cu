@@ -698,7 +698,7 @@ extern "C" iq_status iq_indexer_logits(const uint8_t* q_fp4, const uint8_t* q_sf
   if (st != IQ_OK) return st;
   CUtensorMap tm_k, tm_q;
   if (!encode_2d_u8(&tm_k, k_fp4, iq::kHeadDim / 2, static_cast<uint64_t>(N), 64, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !encode_2d_u8(&tm_q, q_fp4, iq::kHeadDim / 2, static_cast<uint64_t>(M) * iq::kNumHeads, 64, 128,
+      !encode_2d_u8(&tm_q, q_fp4, iq::kHeadDim / 2, static_cast<uint64_t>(M) * iq::kNumHeads, 64, 256,
                     CU_TENSOR_MAP_SWIZZLE_64B)) {
     return IQ_ERR_CUDA;
   }

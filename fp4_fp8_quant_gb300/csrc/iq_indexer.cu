@@ -12,23 +12,27 @@
 //          key index, as int32 indices in ascending order, -1 padded.
 //
 // K5 indexer_logits_kernel.  A dense FP4 contraction, so on the tensor cores:
-// tcgen05.mma kind::mxf4 block_scale (E2M1 x E2M1, UE8M0 per 32 K) with the
-// keys on the MMA's M side (128 per tile) and two query tokens x 64 heads on
-// its N side (128), K = 128 in two MMAs of 64.  Each FP32 accumulator lane is
-// one key and holds all 64 heads of both tokens, so the ReLU and the weighted
-// sum over the heads stay inside one thread of the epilogue.  Warp roles (352
-// threads): warps 0 and 10 decide the tile sequence and fill alternate
-// stages of a 6-stage ring -- key and query tiles by TMA (64-byte rows,
-// 64-byte swizzle), their scale words and the pair's weights by asynchronous
-// copies, the tile's metadata, two end markers after the last tile; warp 1
-// owns tensor memory and issues the scale copies and MMAs of every tile, in
-// order, into three accumulator buffers; warps 2..9, two groups of four (one
-// warp per 32-lane quarter of tensor memory) taking alternate tiles, drain an
-// accumulator and form 32 keys' scores for both tokens from the stage's
-// weights.
-// Tiles (key block, token pair) are dealt to the CTAs in chunks of 8
-// consecutive token pairs of one key block, chunk c to CTA c mod grid; the
-// producer skips the pairs that can see no key of the block.
+// tcgen05.mma kind::mxf4 block_scale (E2M1 x E2M1, UE8M0 per 32 K) in its
+// CTA-pair form.  The keys are the MMA's M side, 256 per instruction (128 in
+// each CTA of the pair); two query tokens x 64 heads are its N side (128),
+// one token's heads in each CTA; K = 128 in two MMAs of 64.  Each accumulator
+// lane of a CTA is one of its keys and holds all 64 heads of both tokens, so
+// the ReLU and the weighted sum over the heads stay inside one thread of the
+// epilogue.  Work comes in chunks of one 256-key block and 16 consecutive
+// query tokens, tile j pairing tokens j and 8 + j: each CTA's query rows for
+// the chunk (8 tokens x 64 heads) are then contiguous and, like the keys, the
+// scale words and the weights, are loaded once per chunk into one of three
+// slots, so the MMA issuer's per-tile work is two MMAs and a commit.  Warp
+// roles (320 threads per CTA): warp 0 stages the slots (TMA with the 64-byte
+// swizzle for keys and queries, a bulk copy for the weights, scale words
+// transposed through registers into the layout tcgen05.cp reads; one
+// cluster-scope arrive per chunk); warp 1 owns tensor memory and, in the
+// leader CTA, issues each chunk's scale copies and its tiles' MMAs in order
+// into three accumulator buffers; warps 2..9, two groups of four (one warp
+// per 32-lane quarter of tensor memory) taking alternate tiles, drain an
+// accumulator and form their 32 keys' scores for both tokens.  Chunks are
+// dealt to the CTA pairs round robin; tiles whose two tokens see no key of
+// the block are skipped.
 //
 // K6 indexer_topk_kernel.  One CTA per query row: radix selection of the k-th
 // largest score over order-preserving 32-bit keys (11, 11, then 10 bits,
@@ -54,47 +58,53 @@ __device__ uint32_t g_iq_status_indexer;
 
 namespace {
 
-constexpr int kKeysPerTile = 128;                    // MMA M
-constexpr int kTokensPerTile = 2;
-constexpr int kRowsB = kTokensPerTile * kNumHeads;   // MMA N = 128
-constexpr int kRowBytes = kHeadDim / 2;              // 64: one packed FP4 head / key
-constexpr int kTileBytes = kKeysPerTile * kRowBytes; // 8 KB, A and B alike
-constexpr int kStages = 6;
+constexpr int kKeysPerCta = 128;                      // MMA M per CTA
+constexpr int kKeysPerTile = 2 * kKeysPerCta;         // 256 keys per pair tile
+constexpr int kChunkTokens = 16;                      // query tokens per chunk
+constexpr int kHalfTokens = kChunkTokens / 2;         // tile j: tokens j (CTA 0) and 8 + j (CTA 1)
+constexpr int kRowsB = 2 * kNumHeads;                 // MMA N = 128
+constexpr int kRowBytes = kHeadDim / 2;               // 64: one packed FP4 head / key
+constexpr int kKeyTileBytes = kKeysPerCta * kRowBytes;     // 8 KB per CTA
+constexpr int kQRows = kHalfTokens * kNumHeads;            // 512 query rows per CTA and chunk
+constexpr int kQBoxRows = 256;                             // rows per tensor-map box
+constexpr int kQTileBytes = kNumHeads * kRowBytes;         // 4 KB: one token's heads
+constexpr int kSlots = 3;                             // chunks in flight
 constexpr int kAccBufs = 3;
-constexpr int kChunkPairs = 8;                       // token pairs per chunk of tiles
-constexpr int kEpiWarps = 8;                         // two groups of four, alternate tiles
+constexpr int kEpiWarps = 12;                         // three groups of four, tile i to group i % 3
 constexpr int kGroupWarps = 4;
-constexpr int kProducerWarp2 = 2 + kEpiWarps;        // the second producer (odd tiles)
-constexpr int kThreads = (3 + kEpiWarps) * 32;
+constexpr int kEpiGroups = kEpiWarps / kGroupWarps;
+static_assert(kEpiGroups == kAccBufs, "each epilogue group drains its own accumulator buffer");
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr uint16_t kPairMask = 0x3;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfaCol = kAccBufs * kRowsB;      // 384 + 8 b
-constexpr uint32_t kSfbCol = kSfaCol + 32;           // 416 + 8 b
-static_assert(kSfbCol + 8 * kAccBufs <= kTmemCols, "tensor memory columns");
+// Scale factors in tensor memory, per slot: the chunk's query scales, 4
+// columns per tile (384 + 32 slot + 4 j), and its key scales (480 + 4 slot),
+// copied when the chunk's MMAs begin.
+constexpr uint32_t kSfbCol = kAccBufs * kRowsB;
+constexpr uint32_t kSfaCol = kSfbCol + kSlots * 4 * kHalfTokens;
+static_assert(kSfaCol + 4 * kSlots <= kTmemCols, "tensor memory columns");
 
-// Shared memory per stage: A tile (keys), B tile (the pair's query heads),
-// their scale words in the tcgen05.cp 32x128b layout (512 B each), the pair's
-// weights (2 x 64 floats) and the tile's metadata.  The producer decides the
-// tile sequence and writes each tile's metadata into its stage; the MMA
-// issuer and the epilogue follow the stages, so only the producer reads the
-// visible lengths.  A stage is released by the MMAs and the four warps of
-// the epilogue group that takes the tile (they read its weights and metadata).
-constexpr int kOffSfa = 2 * kTileBytes;
-constexpr int kOffSfb = kOffSfa + 512;
-constexpr int kOffW = kOffSfb + 512;
-constexpr int kOffMeta = kOffW + kTokensPerTile * kNumHeads * 4;
-constexpr int kStageBytes = 18 * 1024;
-static_assert(kOffMeta + 16 <= kStageBytes && kStageBytes % 1024 == 0, "stage layout");
-constexpr int kOffBar = kStages * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;
+// A slot holds one chunk: this CTA's query rows (8 tokens x 64 heads, 64-byte
+// swizzle), its 128 keys, the key scales and the 8 tiles' query scales (both
+// tokens of each, as every CTA's tensor memory holds the scales of all N rows)
+// in the tcgen05.cp 32x128b layout, the 16 tokens' weights and the metadata.
+constexpr int kSlotQ = 0;
+constexpr int kSlotK = kQRows * kRowBytes;
+constexpr int kSlotSfa = kSlotK + kKeyTileBytes;
+constexpr int kSlotSfb = kSlotSfa + 512;
+constexpr int kSlotW = kSlotSfb + kHalfTokens * 512;
+constexpr int kSlotMeta = kSlotW + kChunkTokens * kNumHeads * 4;   // int[20]
+constexpr int kSlotBytes = 49 * 1024;
+static_assert(kSlotMeta + 20 * 4 <= kSlotBytes && kSlotK % 1024 == 0, "slot layout");
+constexpr int kOffBar = kSlots * kSlotBytes;
+constexpr int kNumBars = 3 * kSlots + 2 * kAccBufs + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-// Two producer warps fill alternate tiles (stage s belongs to producer s % 2).
-// Each completes one of its stages (its last arrive) this many of its own
-// tiles after issuing the stage's asynchronous copies, so their latency
-// overlaps later tiles.
-constexpr int kProducers = 2;
-constexpr int kCopyLag = 2;
-static_assert(kStages % kProducers == 0 && kCopyLag < kStages / kProducers, "a stage's arrive precedes its reuse");
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // over half of an SM: one CTA per SM
+static_assert(kSmemBytes > 114 * 1024 && kSmemBytes <= 227 * 1024, "one CTA per SM");
+static_assert(kOffBar + kNumBars * 8 <= kOffMisc, "barriers");
+// Metadata: [0] the visible tiles (bits 0-7) or kEndChunk, [1] key block,
+// [2] first token, [4 + i] visible length of token i of the chunk.
+constexpr int kEndChunk = 1 << 30;
 
 struct IndexerArgs {
   const uint32_t* k_sf;   // [N] scale words (4 UE8M0 bytes per key)
@@ -104,7 +114,7 @@ struct IndexerArgs {
   float* logits;          // [M][ld]
   long long ld;
   int M, N;
-  int key_blocks, pairs, chunks_per_block, num_chunks;
+  int key_blocks, chunks_per_block, num_chunks;
   unsigned long long timeout_ns;
 };
 
@@ -113,15 +123,34 @@ __device__ __forceinline__ void fail(volatile uint32_t* abort_flag, uint32_t bit
   *abort_flag = 1u;
 }
 
-// Lengths of the 16 tokens of a chunk's 8 pairs, one per lane (lanes 0..15),
-// clamped to [0, N]; 0 past M.
+// Length of token i of chunk ch (lanes 0..15), clamped to [0, N]; 0 past M.
 __device__ __forceinline__ int chunk_lengths(const IndexerArgs& a, int ch, int lane) {
-  if (ch >= a.num_chunks || lane >= 2 * kChunkPairs) return 0;
+  if (ch >= a.num_chunks || lane >= kChunkTokens) return 0;
   const int kb = ch / a.chunks_per_block;
-  const int t = (ch - kb * a.chunks_per_block) * 2 * kChunkPairs + lane;
+  const int t = (ch - kb * a.chunks_per_block) * kChunkTokens + lane;
   if (t >= a.M) return 0;
   const int L = __ldg(a.len + t);
   return L < 0 ? 0 : (L > a.N ? a.N : L);
+}
+
+// Scale words of 128 rows into the tcgen05.cp 32x128b layout (word [r * 4 +
+// c] = row c * 32 + r): lane l holds rows 4l..4l+3 in `v`.
+__device__ __forceinline__ void store_scale_rows(uint32_t* dst, int lane, const uint4& v) {
+  const int c = lane >> 3, r = (lane & 7) * 4;
+  dst[(r + 0) * 4 + c] = v.x;
+  dst[(r + 1) * 4 + c] = v.y;
+  dst[(r + 2) * 4 + c] = v.z;
+  dst[(r + 3) * 4 + c] = v.w;
+}
+
+// Four consecutive scale words from `src`, of which the first `n` exist.
+__device__ __forceinline__ uint4 load_scale_words(const uint32_t* src, int n) {
+  if (n >= 4) return __ldg(reinterpret_cast<const uint4*>(src));
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (n > 0) v.x = __ldg(src);
+  if (n > 1) v.y = __ldg(src + 1);
+  if (n > 2) v.z = __ldg(src + 2);
+  return v;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -130,261 +159,309 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* full = bars;                          // stage s filled (TMA bytes + the producer's arrive)
-  uint64_t* empty = bars + kStages;               // stage s consumed by the MMAs and the epilogue
-  uint64_t* acc_full = bars + 2 * kStages;        // accumulator b complete
-  uint64_t* acc_empty = acc_full + kAccBufs;      // accumulator b drained by the 8 epilogue warps
-  uint64_t* final_bar = acc_empty + kAccBufs;     // every MMA issued by this CTA completed
+  uint64_t* kfull = bars;                         // leader: both CTAs' slots loaded and staged
+  uint64_t* kstaged = bars + kSlots;              // this CTA's slot: metadata written, weights landed
+  uint64_t* kempty = bars + 2 * kSlots;           // the chunk's MMAs and this CTA's epilogue warps are done
+  uint64_t* acc_full = bars + 3 * kSlots;         // accumulator b complete (both CTAs)
+  uint64_t* acc_empty = acc_full + kAccBufs;      // leader: the pair's eight epilogue warps drained b
+  uint64_t* final_bar = acc_empty + kAccBufs;     // every MMA of the pair completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
+  auto slot_ptr = [&](int k) { return smem + k * kSlotBytes; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t timeout = args.timeout_ns;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
 
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_q);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + kGroupWarps);
+    for (int k = 0; k < kSlots; ++k) {
+      mbar_init(&kfull[k], 3);                    // leader's expect-tx arrive + both CTAs' staging arrives
+      mbar_init(&kstaged[k], 1);
+      mbar_init(&kempty[k], 1 + kEpiWarps);
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], kGroupWarps);
+      mbar_init(&acc_empty[b], 2 * kGroupWarps);
     }
     mbar_init(final_bar, 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
   }
+  // Barriers and tensor memory must be ready in both CTAs before either
+  // issues anything that touches the other.
   tc_fence_before_sync();
-  __syncthreads();
+  cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t kfull_l0 = mapa_shared(smem_u32(&kfull[0]), 0);
+  const uint32_t acc_empty_l0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
+  const int pair_id = static_cast<int>(cluster_id_x());
+  const int num_pairs = static_cast<int>(cluster_count_x());
   // The queries' FP4 Q may be the preceding kernel's output.
   grid_dependency_wait();
 
-  if (warp == 0 || warp == kProducerWarp2) {
-    // ----------------------------------------------------------- producers
-    // Tiles: chunks ch = blockIdx.x, + gridDim.x, ...; in each, the token
-    // pairs g0 .. g0 + 7 against key block kb, skipping pairs that cannot
-    // see any key of the block; then two end markers (g = -1).  Both
-    // producers walk the whole sequence; producer p fills the tiles with
-    // it % 2 == p.  A stage's asynchronous copies (scale words, weights) are
-    // waited for kCopyLag of the producer's own tiles later; then the stage is
-    // arrived.
-    const int p = warp == 0 ? 0 : 1;
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // Chunks ch = pair_id, + num_pairs, ... with a visible tile, each into
+    // the next slot: the metadata, the scale words (loaded four rows per
+    // lane, stored transposed into the tcgen05.cp layout), the weights by a
+    // bulk copy on this CTA's slot barrier, the keys and the query rows by
+    // TMA on the leader's; then one cluster-scope arrive on the leader's slot
+    // barrier.  Last, an end chunk.
     uint32_t issued_mask = 0, issued_phase = 0;
-    int it = 0, own = 0;
+    int nchunk = 0;
     bool ok = true;
-    auto complete_stage = [&](int j) {   // global tile j's copies have landed
-      uint8_t* st = smem + (j % kStages) * kStageBytes;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const int g = reinterpret_cast<const volatile int*>(st + kOffMeta)[1];
-        if (g >= 0) {
-          mbar_arrive_expect_tx(&full[j % kStages], 2 * kTileBytes);
-        } else {
-          mbar_arrive(&full[j % kStages]);   // the end marker has no tile loads
-        }
-      }
-    };
-    // Global tile index of this producer's own tile n.
-    auto own_tile = [&](int n) { return n * kProducers + p; };
-    auto stage_tile = [&](int kb, int g, int L0, int L1) -> bool {
-      const int mine = (it % kProducers) == p;
-      const int s = it % kStages;
-      const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-      ++it;
-      if (!mine) return true;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[s], ph ^ 1u, timeout))) {
+    auto next_slot = [&](int& slot, uint32_t& kph) -> bool {
+      slot = nchunk % kSlots;
+      kph = static_cast<uint32_t>(nchunk / kSlots) & 1u;
+      ++nchunk;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&kempty[slot], kph ^ 1u, timeout))) {
         if (lane == 0) fail(abort_flag, kStatusProducerWait);
         return false;
       }
-      uint8_t* st = smem + s * kStageBytes;
-      if (g >= 0) {
-        // Scale words straight into the tcgen05.cp 32x128b layout, word
-        // [r * 4 + c] = row c * 32 + r (lane r copies rows r, 32 + r, ...);
-        // rows past the data zero-filled.  The pair's weights, 16 bytes per lane.
-        uint32_t* sfa = reinterpret_cast<uint32_t*>(st + kOffSfa);
-        uint32_t* sfb = reinterpret_cast<uint32_t*>(st + kOffSfb);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int key = kb * kKeysPerTile + c * 32 + lane;
-          cp_async_4(sfa + lane * 4 + c, args.k_sf + (key < args.N ? key : 0), key < args.N ? 4u : 0u);
-          const long long qrow = static_cast<long long>(g) * kRowsB + c * 32 + lane;
-          const bool qin = qrow < static_cast<long long>(args.M) * kNumHeads;
-          cp_async_4(sfb + lane * 4 + c, args.q_sf + (qin ? qrow : 0), qin ? 4u : 0u);
-        }
-        const bool win = 2 * g + lane / 16 < args.M;
-        cp_async_16(st + kOffW + lane * 16, args.w + (win ? static_cast<long long>(2 * g) * kNumHeads + lane * 4 : 0),
-                    win ? 16u : 0u);
-      }
-      cp_async_commit();
-      if (lane == 0) {
-        *reinterpret_cast<int4*>(st + kOffMeta) = make_int4(kb, g, L0, L1);
-        if (g >= 0) {
-          tma_load_2d(st, &tm_k, &full[s], 0, kb * kKeysPerTile);
-          tma_load_2d(st + kTileBytes, &tm_q, &full[s], 0, g * kRowsB);
-          issued_mask |= 1u << s;
-          issued_phase = (issued_phase & ~(1u << s)) | (ph << s);
-        }
-      }
-      ++own;
-      if (own > kCopyLag) {
-        cp_async_wait<kCopyLag>();
-        complete_stage(own_tile(own - 1 - kCopyLag));
-      }
       return true;
     };
-    int lv = chunk_lengths(args, blockIdx.x, lane);
-    for (int ch = blockIdx.x; ch < args.num_chunks && ok; ch += gridDim.x) {
-      const int lv_next = chunk_lengths(args, ch + gridDim.x, lane);   // in flight during this chunk
+    int lv = chunk_lengths(args, pair_id, lane);
+    for (int ch = pair_id; ch < args.num_chunks && ok; ch += num_pairs) {
+      const int lv_next = chunk_lengths(args, ch + num_pairs, lane);   // in flight during this chunk
       const int kb = ch / args.chunks_per_block;
-      const int gbase = (ch - kb * args.chunks_per_block) * kChunkPairs;
-      for (int j = 0; j < kChunkPairs && ok; ++j) {
-        const int g = gbase + j;
-        const int L0 = __shfl_sync(0xFFFFFFFFu, lv, 2 * j);
-        const int L1 = __shfl_sync(0xFFFFFFFFu, lv, 2 * j + 1);
-        if (g >= args.pairs || kb * kKeysPerTile >= max(L0, L1)) continue;
-        if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) {
-          ok = false;
-          break;
-        }
-        ok = stage_tile(kb, g, L0, L1);
+      const int tb = (ch - kb * args.chunks_per_block) * kChunkTokens;
+      uint32_t vis = 0;   // tiles with a token that sees a key of the block (warp-uniform)
+#pragma unroll
+      for (int j = 0; j < kHalfTokens; ++j) {
+        const int L = max(__shfl_sync(0xFFFFFFFFu, lv, j), __shfl_sync(0xFFFFFFFFu, lv, kHalfTokens + j));
+        if (kb * kKeysPerTile < L) vis |= 1u << j;
       }
+      const int lv_here = lv;
       lv = lv_next;
+      if (vis == 0u) continue;
+      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) {
+        ok = false;
+        break;
+      }
+      int slot;
+      uint32_t kph;
+      if (!(ok = next_slot(slot, kph))) break;
+      uint8_t* ks = slot_ptr(slot);
+      int* meta = reinterpret_cast<int*>(ks + kSlotMeta);
+      if (lane < kChunkTokens) meta[4 + lane] = lv_here;
+      if (lane == 0) {
+        meta[0] = static_cast<int>(vis);
+        meta[1] = kb;
+        meta[2] = tb;
+      }
+      // Scale words: this CTA's 128 keys, then per visible tile its 128
+      // query rows (token tb + j's heads, then token tb + 8 + j's).  Every
+      // load goes out before the first store, so the chunk waits for one
+      // load latency, not nine.
+      uint4 sfw[1 + kHalfTokens];
+      {
+        const int key0 = kb * kKeysPerTile + static_cast<int>(rank) * kKeysPerCta + 4 * lane;
+        sfw[0] = load_scale_words(args.k_sf + (key0 < args.N ? key0 : 0), min(4, args.N - key0));
+      }
+#pragma unroll
+      for (int j = 0; j < kHalfTokens; ++j) {
+        const int t = tb + j + (lane >= 16 ? kHalfTokens : 0);
+        const bool need = ((vis >> j) & 1u) && t < args.M;
+        sfw[1 + j] = load_scale_words(args.q_sf + static_cast<long long>(need ? t : 0) * kNumHeads + 4 * (lane & 15),
+                                      need ? 4 : 0);
+      }
+      store_scale_rows(reinterpret_cast<uint32_t*>(ks + kSlotSfa), lane, sfw[0]);
+#pragma unroll
+      for (int j = 0; j < kHalfTokens; ++j)
+        if ((vis >> j) & 1u) store_scale_rows(reinterpret_cast<uint32_t*>(ks + kSlotSfb + j * 512), lane, sfw[1 + j]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        // Weights of the chunk's tokens that exist (rows past M are never read).
+        const uint32_t wbytes = static_cast<uint32_t>(min(kChunkTokens, args.M - tb) * kNumHeads * 4);
+        mbar_arrive_expect_tx(&kstaged[slot], wbytes);
+        bulk_load(ks + kSlotW, args.w + static_cast<long long>(tb) * kNumHeads, wbytes, &kstaged[slot]);
+        if (leader) mbar_arrive_expect_tx(&kfull[slot], 2 * (kKeyTileBytes + kQRows * kRowBytes));
+        const uint32_t kbar = kfull_l0 + 8u * static_cast<uint32_t>(slot);
+        tma_load_2d_pair(ks + kSlotK, &tm_k, kbar, 0, kb * kKeysPerTile + static_cast<int>(rank) * kKeysPerCta);
+        const int qrow0 = (tb + static_cast<int>(rank) * kHalfTokens) * kNumHeads;
+        tma_load_2d_pair(ks + kSlotQ, &tm_q, kbar, 0, qrow0);
+        tma_load_2d_pair(ks + kSlotQ + kQBoxRows * kRowBytes, &tm_q, kbar, 0, qrow0 + kQBoxRows);
+        mbar_arrive_cluster(kbar);   // this CTA's scale words staged
+        issued_mask |= 1u << slot;
+        issued_phase = (issued_phase & ~(1u << slot)) | (kph << slot);
+      }
     }
-    // Two end markers (g = -1), one for each MMA issuer and epilogue group
-    // (they take alternate tiles), then every own stage still waiting for its
-    // copies.
-    if (ok) ok = stage_tile(0, -1, 0, 0);
-    if (ok) ok = stage_tile(0, -1, 0, 0);
-    cp_async_wait<0>();
-    for (int n = own - kCopyLag > 0 ? own - kCopyLag : 0; n < own; ++n) complete_stage(own_tile(n));
+    // The end chunk: metadata only.
+    if (ok) {
+      int slot;
+      uint32_t kph;
+      if (next_slot(slot, kph)) {
+        if (lane == 0) {
+          reinterpret_cast<volatile int*>(slot_ptr(slot) + kSlotMeta)[0] = kEndChunk;
+          mbar_arrive(&kstaged[slot]);
+          if (leader) mbar_arrive(&kfull[slot]);
+          mbar_arrive_cluster(kfull_l0 + 8u * static_cast<uint32_t>(slot));
+        }
+      }
+    }
+    // Teardown: the pair's MMAs read this CTA's slots; wait (bounded) until
+    // every loaded slot was released.
     if (lane == 0) {
-      for (int s = 0; s < kStages; ++s)
-        if (((issued_mask >> s) & 1u) && !mbar_wait(&empty[s], (issued_phase >> s) & 1u, 2 * timeout))
+      for (int k = 0; k < kSlots; ++k)
+        if (((issued_mask >> k) & 1u) && !mbar_wait(&kempty[k], (issued_phase >> k) & 1u, 2 * timeout))
           fail(abort_flag, kStatusTeardownWait);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // One issuer takes every tile in order, so that each tile's MMAs depend
-    // only on earlier tiles: with two issuers on alternate tiles sharing the
-    // three accumulator buffers, the two halves of the pipeline could end up
-    // waiting on each other.  It passes both end markers on, then stops.
+    // ------------------------------------------------- MMA issuer (leader)
+    // Chunk by chunk: the scale copies, then per visible tile two MMAs into
+    // the next accumulator buffer; the slot is released after the chunk's
+    // last MMAs.
     if (lane == 0) {
-      const uint32_t idesc_k0 = idesc_mxf4_e2m1(kKeysPerTile, kRowsB, 0, 0);
-      const uint32_t idesc_k1 = idesc_mxf4_e2m1(kKeysPerTile, kRowsB, 2, 2);
-      int markers = 0;
-      for (int it = 0;; ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-        const int b = it % kAccBufs;
-        const uint32_t aph = static_cast<uint32_t>(it / kAccBufs) & 1u;
-        if (*abort_flag) break;
-        if (!mbar_wait(&full[s], ph, timeout) || !mbar_wait(&acc_empty[b], aph ^ 1u, timeout)) {
-          fail(abort_flag, kStatusMmaWait);
-          break;
+      if (leader) {
+        const uint32_t idesc_k0 = idesc_mxf4_e2m1(kKeysPerTile, kRowsB, 0, 0);
+        const uint32_t idesc_k1 = idesc_mxf4_e2m1(kKeysPerTile, kRowsB, 2, 2);
+        int it = 0;
+        for (int n = 0;; ++n) {
+          const int slot = n % kSlots;
+          if (*abort_flag) break;
+          if (!mbar_wait(&kfull[slot], static_cast<uint32_t>(n / kSlots) & 1u, timeout)) {
+            fail(abort_flag, kStatusMmaWait);
+            break;
+          }
+          tc_fence_after_sync();
+          const uint8_t* ks = slot_ptr(slot);
+          const int vis = reinterpret_cast<const volatile int*>(ks + kSlotMeta)[0];
+          if (vis & kEndChunk) break;
+          const uint32_t sfa = tmem + kSfaCol + 4u * static_cast<uint32_t>(slot);
+          const uint32_t sfb0 = tmem + kSfbCol + 4u * kHalfTokens * static_cast<uint32_t>(slot);
+          tc_cp_32x128b_warpx4_pair(sfa, smem_desc_sf(smem_u32(ks + kSlotSfa)));
+          for (int j = 0; j < kHalfTokens; ++j)
+            if ((vis >> j) & 1)
+              tc_cp_32x128b_warpx4_pair(sfb0 + 4u * j, smem_desc_sf(smem_u32(ks + kSlotSfb + j * 512)));
+          const uint64_t adesc = smem_desc_sw64(smem_u32(ks + kSlotK));
+          bool ok = true;
+          for (int j = 0; j < kHalfTokens && ok; ++j) {
+            if (!((vis >> j) & 1)) continue;
+            const int b = it % kAccBufs;
+            const uint32_t aph = static_cast<uint32_t>(it / kAccBufs) & 1u;
+            ++it;
+            if (!mbar_wait(&acc_empty[b], aph ^ 1u, timeout)) {
+              fail(abort_flag, kStatusMmaWait);
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint64_t bdesc = smem_desc_sw64(smem_u32(ks + kSlotQ + j * kQTileBytes));
+            const uint32_t d = tmem + static_cast<uint32_t>(b * kRowsB);
+            const uint32_t sfb = sfb0 + 4u * static_cast<uint32_t>(j);
+            // K = 128: dims 0..63 (scale bytes 0, 1), then dims 64..127 (bytes
+            // 2, 3), 32 bytes further along each 64-byte row.
+            tc_mma_mxf4_pair(d, adesc, bdesc, idesc_k0, sfa, sfb, 0u);
+            tc_mma_mxf4_pair(d, adesc + 2, bdesc + 2, idesc_k1, sfa, sfb, 1u);
+            tc_commit_pair(&acc_full[b], kPairMask);
+          }
+          if (!ok) break;
+          tc_commit_pair(&kempty[slot], kPairMask);
         }
-        tc_fence_after_sync();
-        uint8_t* st = smem + s * kStageBytes;
-        const int g = reinterpret_cast<const volatile int*>(st + kOffMeta)[1];
-        if (g >= 0) {
-          const uint32_t sfa = tmem + kSfaCol + 8u * b;
-          const uint32_t sfb = tmem + kSfbCol + 8u * b;
-          tc_cp_32x128b_warpx4(sfa, smem_desc_sf(smem_u32(st + kOffSfa)));
-          tc_cp_32x128b_warpx4(sfb, smem_desc_sf(smem_u32(st + kOffSfb)));
-          const uint64_t adesc = smem_desc_sw64(smem_u32(st));
-          const uint64_t bdesc = smem_desc_sw64(smem_u32(st + kTileBytes));
-          const uint32_t d = tmem + static_cast<uint32_t>(b * kRowsB);
-          // K = 128: dims 0..63 (scale bytes 0, 1), then dims 64..127 (bytes 2,
-          // 3), 32 bytes further along each 64-byte row.
-          tc_mma_mxf4(d, adesc, bdesc, idesc_k0, sfa, sfb, 0u);
-          tc_mma_mxf4(d, adesc + 2, bdesc + 2, idesc_k1, sfa, sfb, 1u);
-        }
-        tc_commit(&empty[s]);
-        tc_commit(&acc_full[b]);   // also passes an end marker on to the epilogue
-        if (g < 0 && ++markers == 2) break;
+        tc_commit_pair(final_bar, kPairMask);
       }
-      tc_commit(final_bar);
+      // Both CTAs: every pair MMA that uses this CTA's memory has completed.
       if (!mbar_wait(final_bar, 0, 2 * timeout)) fail(abort_flag, kStatusTeardownWait);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // Group (warp - 2) / 4 takes the tiles of its parity; each warp drains
-    // TMEM lanes 32 quad .. 32 quad + 31 (32 keys) for both tokens.
+    // The same chunk walk; group (warp - 2) / 4 takes visible tile i
+    // (counted over all chunks) when i % 3 is its index, and with it
+    // accumulator buffer i % 3; each warp drains TMEM lanes 32 quad ..
+    // 32 quad + 31 (32 keys), one token (64 columns) at a time; after a chunk
+    // every warp releases the slot.
     const int quad = warp & 3;
     const int group = (warp - 2) >> 2;
-    for (int it = group;; it += 2) {
-      const int s = it % kStages;
-      const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-      const int b = it % kAccBufs;
-      const uint32_t aph = static_cast<uint32_t>(it / kAccBufs) & 1u;
+    int it = 0;
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int slot = n % kSlots;
       if (*abort_flag) break;
-      // acc_full: the MMAs are done; full: the producer's writes to the stage
-      // (metadata, weights) are visible to this thread.
-      const bool got = mbar_wait(&acc_full[b], aph, timeout) && mbar_wait(&full[s], ph, timeout);
+      const bool got = mbar_wait(&kstaged[slot], static_cast<uint32_t>(n / kSlots) & 1u, timeout);
       if (!got) fail(abort_flag, kStatusEpilogueWait);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
-      const uint8_t* st = smem + s * kStageBytes;
-      const int4 meta = *reinterpret_cast<const int4*>(st + kOffMeta);
-      if (meta.y < 0) break;
-      tc_fence_after_sync();
-      float v[kRowsB];
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(b * kRowsB);
-      tmem_ld_32x32b_x32(taddr, v);
-      tmem_ld_32x32b_x32(taddr + 32, v + 32);
-      tmem_ld_32x32b_x32(taddr + 64, v + 64);
-      tmem_ld_32x32b_x32(taddr + 96, v + 96);
-      tmem_ld_wait(v);
-      tmem_ld_wait(v + 32);
-      tmem_ld_wait(v + 64);
-      tmem_ld_wait(v + 96);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[b]);
-      const int key = meta.x * kKeysPerTile + quad * 32 + lane;
-      // Per token: sum_h w_h max(0, d_h), two heads per packed FMA in four
-      // independent chains; the weights are the same for the whole warp
-      // (broadcast reads).
-      float score[kTokensPerTile];
-#pragma unroll
-      for (int tok = 0; tok < kTokensPerTile; ++tok) {
-        const float4* wv = reinterpret_cast<const float4*>(st + kOffW) + tok * (kNumHeads / 4);
-        const float* d = v + tok * kNumHeads;
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};   // packed (+0, +0)
-#pragma unroll
-        for (int i = 0; i < kNumHeads / 4; ++i) {
-          const float4 wq = wv[i];
-          acc[i & 3] = f2_fma(f2_pack(fmaxf(d[4 * i], 0.f), fmaxf(d[4 * i + 1], 0.f)), f2_pack(wq.x, wq.y), acc[i & 3]);
-          acc[(i + 2) & 3] =
-              f2_fma(f2_pack(fmaxf(d[4 * i + 2], 0.f), fmaxf(d[4 * i + 3], 0.f)), f2_pack(wq.z, wq.w), acc[(i + 2) & 3]);
+      const uint8_t* ks = slot_ptr(slot);
+      const int* meta = reinterpret_cast<const int*>(ks + kSlotMeta);
+      const int vis = meta[0];
+      if (vis & kEndChunk) break;
+      const int kb = meta[1], tb = meta[2];
+      const int key = kb * kKeysPerTile + static_cast<int>(rank) * kKeysPerCta + quad * 32 + lane;
+      for (int j = 0; j < kHalfTokens; ++j) {
+        if (!((vis >> j) & 1)) continue;
+        const int b = it % kAccBufs;
+        const uint32_t aph = static_cast<uint32_t>(it / kAccBufs) & 1u;
+        const bool mine = b == group;
+        ++it;
+        if (!mine) continue;
+        const bool acc = mbar_wait(&acc_full[b], aph, timeout);
+        if (!acc) fail(abort_flag, kStatusEpilogueWait);
+        if (!__all_sync(0xFFFFFFFFu, acc)) {
+          ok = false;
+          break;
         }
-        const uint64_t sum = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
-        float lo, hi;
-        f2_unpack(sum, lo, hi);
-        score[tok] = lo + hi;
+        tc_fence_after_sync();
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(b * kRowsB);
+        // Per token: sum_h w_h max(0, d_h), two heads per packed FMA in four
+        // independent chains; the weights are the same for the whole warp
+        // (broadcast reads).  Columns 0..63: token tb + j; 64..127: tb + 8 + j.
+        // The accumulator is released once the second token's columns are in
+        // registers.
+        float score[2];
+#pragma unroll
+        for (int tok = 0; tok < 2; ++tok) {
+          float d[kNumHeads];
+          tmem_ld_32x32b_x32(taddr + tok * kNumHeads, d);
+          tmem_ld_32x32b_x32(taddr + tok * kNumHeads + 32, d + 32);
+          tmem_ld_wait(d);
+          tmem_ld_wait(d + 32);
+          if (tok == 1) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(acc_empty_l0 + 8u * static_cast<uint32_t>(b));
+          }
+          const float4* wv = reinterpret_cast<const float4*>(ks + kSlotW) + (j + tok * kHalfTokens) * (kNumHeads / 4);
+          uint64_t accv[4] = {0ull, 0ull, 0ull, 0ull};   // packed (+0, +0)
+#pragma unroll
+          for (int i = 0; i < kNumHeads / 4; ++i) {
+            const float4 wq = wv[i];
+            accv[i & 3] =
+                f2_fma(f2_pack(fmaxf(d[4 * i], 0.f), fmaxf(d[4 * i + 1], 0.f)), f2_pack(wq.x, wq.y), accv[i & 3]);
+            accv[(i + 2) & 3] = f2_fma(f2_pack(fmaxf(d[4 * i + 2], 0.f), fmaxf(d[4 * i + 3], 0.f)),
+                                       f2_pack(wq.z, wq.w), accv[(i + 2) & 3]);
+          }
+          const uint64_t sum = f2_add(f2_add(accv[0], accv[1]), f2_add(accv[2], accv[3]));
+          float lo, hi;
+          f2_unpack(sum, lo, hi);
+          score[tok] = lo + hi;
+        }
+        const int L0 = meta[4 + j], L1 = meta[4 + kHalfTokens + j];
+        if (key < L0) args.logits[static_cast<long long>(tb + j) * args.ld + key] = score[0];
+        if (key < L1) args.logits[static_cast<long long>(tb + kHalfTokens + j) * args.ld + key] = score[1];
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);   // this warp is done with the stage
-      if (key < meta.z) args.logits[static_cast<long long>(2 * meta.y) * args.ld + key] = score[0];
-      if (key < meta.w) args.logits[static_cast<long long>(2 * meta.y + 1) * args.ld + key] = score[1];
+      if (ok && lane == 0) mbar_arrive(&kempty[slot]);   // this warp is done with the slot
     }
   }
 
+  // Neither CTA leaves (or frees tensor memory) while the pair may still use
+  // its shared memory, barriers or tensor memory.
   tc_fence_before_sync();
-  __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
@@ -539,12 +616,52 @@ __global__ void __launch_bounds__(kTopkThreads)
 
 }  // namespace
 
+// Clusters of two (the MMA's CTA pairs), plus programmatic stream
+// serialization: the kernel may start while the preceding kernel (the one
+// that wrote the queries) runs; it waits for it before reading anything.
+cudaLaunchConfig_t logits_config(int pairs, cudaLaunchAttribute* attr, cudaStream_t stream) {
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+
+// CTA pairs of the logits kernel that fit at once, per device (set-up).
+constexpr int kMaxIndexerDevices = 64;
+int g_indexer_max_pairs[kMaxIndexerDevices] = {};
+
+int* indexer_pairs_slot() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxIndexerDevices) return nullptr;
+  return &g_indexer_max_pairs[dev];
+}
+
 cudaError_t indexer_setup_device() {
-  const cudaError_t err =
+  cudaError_t err =
       cudaFuncSetAttribute(indexer_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err != cudaSuccess) return err;
-  return cudaFuncSetAttribute(indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kTopkCacheMax * static_cast<int>(sizeof(uint32_t)));
+  err = cudaFuncSetAttribute(indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTopkCacheMax * static_cast<int>(sizeof(uint32_t)));
+  if (err != cudaSuccess) return err;
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = logits_config(1, attr, nullptr);
+  int pairs = 0;
+  err = cudaOccupancyMaxActiveClusters(&pairs, indexer_logits_kernel, &cfg);
+  if (err != cudaSuccess) return err;
+  int* slot = indexer_pairs_slot();
+  if (pairs < 1 || slot == nullptr) return cudaErrorInvalidConfiguration;
+  *slot = pairs;
+  return cudaSuccess;
 }
 
 cudaError_t launch_indexer_logits(const CUtensorMap& tm_k, const CUtensorMap& tm_q, const uint8_t* q_sf,
@@ -560,21 +677,15 @@ cudaError_t launch_indexer_logits(const CUtensorMap& tm_k, const CUtensorMap& tm
   a.M = M;
   a.N = N;
   a.key_blocks = (N + kKeysPerTile - 1) / kKeysPerTile;
-  a.pairs = (M + 1) / 2;
-  a.chunks_per_block = (a.pairs + kChunkPairs - 1) / kChunkPairs;
+  a.chunks_per_block = (M + kChunkTokens - 1) / kChunkTokens;
   a.num_chunks = a.key_blocks * a.chunks_per_block;
   a.timeout_ns = timeout_ns;
-  const int grid = a.num_chunks < sm_count ? a.num_chunks : sm_count;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  (void)sm_count;
+  const int* slot = indexer_pairs_slot();
+  if (slot == nullptr || *slot < 1) return cudaErrorInitializationError;
+  const int pairs = a.num_chunks < *slot ? a.num_chunks : *slot;
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = logits_config(pairs, attr, stream);
   return cudaLaunchKernelEx(&cfg, indexer_logits_kernel, tm_k, tm_q, a);
 }
 
