@@ -83,6 +83,21 @@ def test_topk_selection_is_exact_on_given_scores(cuda_device, k):
     assert np.array_equal(got, want)
 
 
+def test_topk_long_rows_are_exact(cuda_device):
+    """Rows longer than the kernel's shared-memory row cache (12288 keys),
+    with and without ties in the first digit's threshold bin."""
+    rng = np.random.default_rng(77)
+    M, N, k = 5, 20000, 2048
+    s = rng.standard_normal((M, N)).astype(np.float32)
+    s[1] = rng.integers(-3, 4, N).astype(np.float32)       # a few values: the threshold bin overflows the gather
+    s[2] = np.float32(2.0)
+    s[3, 5000:] = -np.inf
+    L = np.array([N, N, N, 15000, 12289], np.int32)
+    got = _topk(s, L, k)
+    want = O.indexer_topk(s.astype(np.float64), L, k)
+    assert np.array_equal(got, want)
+
+
 def test_indexer_prefill_chain_end_to_end(cuda_device):
     """Q from iq_prepare_q on the 4632-token prefill workload, a 4632-key
     cache, causal lengths, top-2048: sampled rows of the logits against the
