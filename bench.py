@@ -609,6 +609,15 @@ def run_ours(args):
             f()
         c_ms = flushed_ms(None, lambda i: fns[i % len(fns)](), reps)
         cbb, cbb_total = time_back_to_back(fns, reps, 2 * len(sets))
+        graph = {}
+        if Ms <= 4632:
+            # Per call inside a 16-call CUDA graph (no per-call launch or event
+            # overhead): over the rotating sets (W and inputs from HBM), and
+            # one set repeated (W in L2, as consecutive calls of a layer see it).
+            graph = {"graph_us_per_call_rotated": graph_us_per_call([fns[i % len(fns)] for i in range(16)], 800),
+                     "graph_us_per_call_w_in_l2": graph_us_per_call([fns[0]] * 16, 800)}
+            graph["graph_frac_of_fp8_peak_rotated"] = (
+                Ms * FLOPS_PER_TOKEN / (graph["graph_us_per_call_rotated"] * 1e-6) / 1e12 / fp8_peak_tflops)
         del sets, fns, lat_s
         xq_in = bf16_input(Ms, K_QUANT)
         qsets = []
@@ -631,7 +640,7 @@ def run_ours(args):
             "quant7168_back_to_back_gbs": qbytes / (qbb_total / reps * 1e-3) / 1e9,
             "chain_tflops": flops / (cm * 1e-3) / 1e12, "chain_frac_of_fp8_peak": flops / (cm * 1e-3) / 1e12 / fp8_peak_tflops,
             "quant7168_us": qs_ms * 1e3, "quant7168_gbs": qbytes / (qs_ms * 1e-3) / 1e9,
-            "quant7168_frac_of_hbm": qbytes / (qs_ms * 1e-3) / 1e9 / hbm_peak}
+            "quant7168_frac_of_hbm": qbytes / (qs_ms * 1e-3) / 1e9 / hbm_peak, **graph}
     # The quantizer's fraction also against the best rate any of its launches
     # reached in this run (the copy-measured peak is not a ceiling for it).
     best_q = max([q_gbs] + [v["quant7168_gbs"] for v in sweep.values()])

@@ -37,15 +37,18 @@ std::atomic<int> g_small_m_max{iq::kSmallMMax};
 std::atomic<int> g_tile_n_override{0};   // 0: by token count; else 128 or 256
 std::atomic<int> g_order_override{0};    // 0: default; 1 feature-major; 2 token-major; 3 interleaved
 
-// Tile width and order of the CTA-pair kernel.  Measured on GB300 (kernel
-// alone, L2 flushed, 65 ... 65536 tokens): the two-head tile is as fast as
-// the one-head tile up to 256 tokens and faster from 512 (up to 1.7x at
-// large M, where the one-head tile moves half again as many operand bytes
-// from L2 per FLOP); token-major order is as fast or faster at every size,
-// by 4 % at 4632 tokens and 16 % at 65536.
-int gemm_tile_n(int) {
+// Tile width and order of the CTA-pair kernel.  Measured on GB300: up to
+// 256 tokens (one 256-row block) the one-head tile spreads the work over 64
+// pairs instead of 32 and is faster per call when calls run back to back
+// (10.2 against 11.7 us at 128 tokens, 10.6 against 11.8 at 256, inside CUDA
+// graphs); from 512 tokens the two-head tile is faster (up to 1.7x at large
+// M, where the one-head tile moves half again as many operand bytes from L2
+// per FLOP).  Token-major order is as fast or faster at every size, by 4 % at
+// 4632 tokens and 16 % at 65536.
+int gemm_tile_n(int M) {
   const int o = g_tile_n_override.load(std::memory_order_relaxed);
-  return o == 128 ? 128 : 256;
+  if (o == 128 || o == 256) return o;
+  return M <= 256 ? 128 : 256;
 }
 
 int gemm_order(int) {

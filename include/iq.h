@@ -127,9 +127,9 @@ int iq_set_small_m_threshold(int max_tokens);
 int iq_small_m_threshold(void);
 
 /* Tuning override of the CTA-pair kernel's tiling, for measurements.  By
- * default the kernel takes two heads (256 output features) per pair tile and
- * orders the pair tiles token-major (consecutive tiles of a CTA pair share
- * their 256 token rows).  tile_n: 128 (one head per tile, two accumulators
+ * default the kernel takes one head (128 output features) per pair tile up to
+ * 256 tokens and two heads (256) above, and orders the pair tiles token-major
+ * (consecutive tiles of a CTA pair share their 256 token rows).  tile_n: 128 (one head per tile, two accumulators
  * in tensor memory) or 256 forces that width, any other value restores the
  * default; order: 1 forces feature-major (consecutive tiles share their
  * heads), 2 token-major, 3 interleaved (token-major tiles dealt round-robin
