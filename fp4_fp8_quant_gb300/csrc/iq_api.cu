@@ -178,7 +178,7 @@ iq_status gemm_stage(const void* xq, const int32_t* x_sf, int M, const void* wq,
   a.m_al = (M + 3) / 4 * 4;
   a.num_m_tiles = (M + 127) / 128;
   a.num_m_pairs = (a.num_m_tiles + iq::gemm_pair_size() - 1) / iq::gemm_pair_size();
-  const int tile_n = gemm_tile_n(M);
+  const int tile_n = fuse != nullptr ? 256 : gemm_tile_n(M);   // the fused instance has two-head tiles
   a.num_pair_tiles = a.num_m_pairs * (iq::kQDim / tile_n);
   a.order = gemm_order(M);
   a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
@@ -246,7 +246,7 @@ iq_status prepare_impl(const void* latent, int M, const void* wq, const uint8_t*
   // With the fusion switched on, the CTA-pair route quantizes the token rows
   // inside the GEMM kernel (one launch); otherwise the quantizer runs first.
   if (g_quant_fusion.load(std::memory_order_relaxed) != 0 && M > g_small_m_max.load(std::memory_order_relaxed) &&
-      gemm_tile_n(M) == 256) {
+      g_tile_n_override.load(std::memory_order_relaxed) != 128) {
     const FusedQuant fuse{latent, reinterpret_cast<unsigned long long*>(xq + prepare_counters_offset(M))};
     return gemm_stage(xq, x_sf, M, wq, wq_sf, pos, q_fp4, q_sf, q_pre, fmt, max_pairs, stream, &fuse);
   }

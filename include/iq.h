@@ -143,8 +143,9 @@ void iq_set_gemm_tiling(int tile_n, int order);
  * stand-alone quantizer, then the GEMM kernel) or on (1: one launch, see
  * iq_prepare_q).  Results are the same either way; on GB300 the fused launch
  * measured slower at every token count, so it is off unless asked for.  The
- * fusion also needs two-head tiles (see iq_set_gemm_tiling).  Process-wide;
- * applies to later calls; returns the previous setting. */
+ * fused launch always takes two-head tiles; forcing one-head tiles
+ * (iq_set_gemm_tiling) turns it off.  Process-wide; applies to later calls;
+ * returns the previous setting. */
 int iq_set_quant_fusion(int on);
 
 /* Diagnostics: the fused quantizer's warps wait ns nanoseconds (at most 1 ms)
