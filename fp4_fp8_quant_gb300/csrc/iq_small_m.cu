@@ -285,11 +285,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     tok_pos[j] =
         (tok_valid[j] && lane < 16) ? static_cast<float>(static_cast<int>(ld_dependent_u32(args.pos + tok_index[j]))) : 0.f;
   }
-  float fhi[4], flo[4];
+  // The RoPE rotation of each token's dims (lanes 0..15), computed while the
+  // MMAs run: cos and (sign-adjusted) sin of angle = position * frequency.
+  // The angle is reduced in turns with a two-float product of position and
+  // frequency (the rounding to an integer uses the 1.5 * 2^23 shift, exact
+  // for |turns| < 2^22), then scaled to radians in [-pi, pi].
+  const float rope_sign = lane < 8 ? -1.f : 1.f;
+  float rcos[kTokPerWarp][4], rsin[kTokPerWarp][4];
+  {
+    float fhi[4], flo[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    fhi[k] = args.rope.hi[4 * (lane & 7) + k];
-    flo[k] = args.rope.lo[4 * (lane & 7) + k];
+    for (int k = 0; k < 4; ++k) {
+      fhi[k] = args.rope.hi[4 * (lane & 7) + k];
+      flo[k] = args.rope.lo[4 * (lane & 7) + k];
+    }
+#pragma unroll
+    for (int j = 0; j < kTokPerWarp; ++j) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float th = __fmul_rn(tok_pos[j], fhi[k]);
+        float tl = __fmaf_rn(tok_pos[j], fhi[k], -th);
+        tl = __fmaf_rn(tok_pos[j], flo[k], tl);
+        const float rn = __fsub_rn(__fadd_rn(th, 12582912.0f), 12582912.0f);
+        const float ang = __fmul_rn(__fadd_rn(__fsub_rn(th, rn), tl), kTwoPi);
+        float sn, cs;
+        __sincosf(ang, &sn, &cs);
+        rcos[j][k] = cs;
+        rsin[j][k] = rope_sign * sn;
+      }
+    }
   }
 
   // (1) This CTA's partial sums over its K half: TMEM lane d = dim d of the
@@ -351,7 +375,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (3) Per token one warp: lane l holds dims 4l..4l+3 of the head.  A warp
   // takes its kTokPerWarp tokens (slots warp, warp + 8, ...) together, so the
   // shuffle and sincos latencies of one token overlap those of the others.
-  const float rope_sign = lane < 8 ? -1.f : 1.f;
   float x[kTokPerWarp][4];
 #pragma unroll
   for (int j = 0; j < kTokPerWarp; ++j) {
@@ -365,9 +388,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tok_valid[0]) {   // warp-uniform; token j is valid only if token 0 is
     // NeoX RoPE on dims 0..63 (lanes 0..15): x1' = x1 c - x2 s, x2' = x2 c + x1 s.
-    // The angle is reduced in turns with a two-float product of position and
-    // frequency (the rounding to an integer uses the 1.5 * 2^23 shift, exact
-    // for |turns| < 2^22), then scaled to radians in [-pi, pi].
 #pragma unroll
     for (int j = 0; j < kTokPerWarp; ++j) {
       float y[4];
@@ -375,16 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < 4; ++k) y[k] = __shfl_xor_sync(0xFFFFFFFFu, x[j][k], 8);
       if (lane < 16) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float th = __fmul_rn(tok_pos[j], fhi[k]);
-          float tl = __fmaf_rn(tok_pos[j], fhi[k], -th);
-          tl = __fmaf_rn(tok_pos[j], flo[k], tl);
-          const float rn = __fsub_rn(__fadd_rn(th, 12582912.0f), 12582912.0f);
-          const float ang = __fmul_rn(__fadd_rn(__fsub_rn(th, rn), tl), kTwoPi);
-          float sn, cs;
-          __sincosf(ang, &sn, &cs);
-          x[j][k] = __fmaf_rn(x[j][k], cs, __fmul_rn(y[k], rope_sign * sn));
-        }
+        for (int k = 0; k < 4; ++k) x[j][k] = __fmaf_rn(x[j][k], rcos[j][k], __fmul_rn(y[k], rsin[j][k]));
       }
     }
     // Fast Walsh-Hadamard transform in Sylvester order (unscaled): dim bits 0
