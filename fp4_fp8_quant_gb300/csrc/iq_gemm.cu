@@ -36,7 +36,10 @@
 //               MMAs slow the tensor pipe on GB300; the packed forms do not),
 //               and stages the FP4 codes in shared memory, from where two bulk
 //               tensor stores per tile write them.  The FP32 pre-quant Q never
-//               touches memory unless the debug output is requested.
+//               touches memory unless the debug output is requested.  With
+//               one-head tiles two warps share each (token, head): each
+//               transforms one half of the dims in place in tensor memory and
+//               reads the other half back for the last Hadamard stage.
 //
 // Scale factors.  The activation scales are per 1x128 block and the weight
 // scales per 128x128 block, but the MMA applies one scale per 32 K: every
@@ -171,20 +174,14 @@ __device__ __forceinline__ int unit_owner(long long u, long long units, int G) {
   return static_cast<int>(((u + 1) * G - 1) / units);
 }
 
-// RoPE, Hadamard, FP4 for one (token, head).  p[j] holds dims (2j, 2j+1) of
-// the 128 FP32 GEMM outputs as one packed pair.  The FP4 codes go to
-// `stage_row`, this row's 64 bytes of the shared staging tile, stored with the
-// 64-byte swizzle of the bulk tensor store (16-byte chunk c of row r at chunk
-// c ^ ((r >> 1) & 3)): a warp's 16-byte writes then fall on distinct banks.
-template <int kFmt>
-__device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int head, int pos, const GemmArgs& args,
-                                             uint8_t* stage_row, int swz) {
-  // NeoX RoPE on dims 0..63: pairs (i, i+32), angle = pos * 10000^(-i/32).
-  // The angle is reduced in turns with a two-float product (head and tail of
-  // the frequency, exact FMA residue) so that it stays accurate for large
-  // positions; the reduced angle lies in [-pi, pi].  Frequencies i and i+1 go
-  // through the packed lanes together; rounding to an integer uses the
-  // 1.5 * 2^23 shift, exact for |turns| < 2^22.
+// NeoX RoPE on dims 0..63 of a (token, head), held as p[0..31] (p[j] = dims
+// 2j, 2j+1 as one packed pair): pairs (i, i+32), angle = pos * 10000^(-i/32).
+// The angle is reduced in turns with a two-float product (head and tail of
+// the frequency, exact FMA residue) so that it stays accurate for large
+// positions; the reduced angle lies in [-pi, pi].  Frequencies i and i+1 go
+// through the packed lanes together; rounding to an integer uses the
+// 1.5 * 2^23 shift, exact for |turns| < 2^22.
+__device__ __forceinline__ void rope_neox64(uint64_t* p, int pos, const GemmArgs& args) {
   const float pf = static_cast<float>(pos);
   const uint64_t pp = f2_pack(pf, pf);
   const uint64_t shift = f2_pack(12582912.0f, 12582912.0f);
@@ -208,20 +205,25 @@ __device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int hea
     p[i >> 1] = f2_fma(x1, c, f2_mul(x2, f2_neg(s)));        // x1 c - x2 s
     p[(i >> 1) + 16] = f2_fma(x2, c, f2_mul(x1, s));         // x2 c + x1 s
   }
-  // Fast Walsh-Hadamard transform in Sylvester order (unscaled).  The stage
-  // pairing dims that differ in bit 0 works inside each packed pair:
-  // (a, b) -> (a + b, a - b) = (a, b) * (1, -1) + (b, a).
+}
+
+// Unscaled fast Walsh-Hadamard stages in Sylvester order over the 2 kN dims
+// held in p[0..kN) (dim bits 0 .. log2(2 kN) - 1, lowest bit first).  The
+// stage pairing dims that differ in bit 0 works inside each packed pair:
+// (a, b) -> (a + b, a - b) = (a, b) * (1, -1) + (b, a).
+template <int kN>
+__device__ __forceinline__ void fwht_packed(uint64_t* p) {
   const uint64_t one_neg = f2_pack(1.0f, -1.0f);
 #pragma unroll
-  for (int j = 0; j < 64; ++j) {
+  for (int j = 0; j < kN; ++j) {
     float a, b;
     f2_unpack(p[j], a, b);
     p[j] = f2_fma(p[j], one_neg, f2_pack(b, a));
   }
 #pragma unroll
-  for (int h = 1; h < 64; h <<= 1) {
+  for (int h = 1; h < kN; h <<= 1) {
 #pragma unroll
-    for (int j = 0; j < 64; ++j) {
+    for (int j = 0; j < kN; ++j) {
       if ((j & h) == 0) {
         const uint64_t a = p[j], b = p[j + h];
         p[j] = f2_add(a, b);
@@ -229,14 +231,19 @@ __device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int hea
       }
     }
   }
-  // FP4 of z = v / sqrt(128), per block of the variant.
-  uint32_t codes[16];
+}
+
+// FP4 of z = v / sqrt(128) for the 2 kN Hadamard outputs in p[0..kN), whole
+// blocks of the variant: codes[w] holds dims 8w..8w+7 as E2M1 nibbles, and
+// byte b of the result is block b's scale.
+template <int kFmt, int kN>
+__device__ __forceinline__ uint64_t fp4_blocks(const uint64_t* p, uint32_t* codes) {
+  uint64_t sfb = 0;
   if constexpr (kFmt != kFp4Nv) {
     // MXFP4: per 32-block UE8M0 exponent e; codes = E2M1(z * 2^-e), formed
     // as v * (2^-e / sqrt(128)), equal to fp32(z) * 2^-e.
-    uint32_t sfw = 0;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < kN / 16; ++b) {
       float amax = 0.f;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
@@ -254,19 +261,16 @@ __device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int hea
         for (int j = 0; j < 4; ++j) f2_unpack(f2_mul(p[16 * b + 4 * t + j], kk), q[2 * j], q[2 * j + 1]);
         codes[4 * b + t] = cvt_e2m1x8(q);
       }
-      sfw |= static_cast<uint32_t>(e + 127) << (8 * b);
+      sfb |= static_cast<uint64_t>(e + 127) << (8 * b);
     }
-    *reinterpret_cast<uint32_t*>(args.q_sf + static_cast<long long>(row) * Fp4Layout<kFmt>::kScaleBytesPerToken +
-                                 head * 4) = sfw;
   } else {
     // NVFP4-style: per 16-block E4M3 scale s = E4M3(max(amax_z, 1e-4) / 6);
     // codes = E2M1(v * (1/s) / sqrt(128)).  Two blocks at a time in packed
     // arithmetic; the reciprocal comes from the scale's code (no division).
     const uint64_t c2 = f2_pack(kInvSqrt128, kInvSqrt128);
     const uint64_t sixth = f2_pack(kSixth, kSixth);
-    uint32_t sfw[2] = {0u, 0u};
 #pragma unroll
-    for (int b = 0; b < 8; b += 2) {
+    for (int b = 0; b < kN / 8; b += 2) {
       float am[2] = {0.f, 0.f};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -296,26 +300,63 @@ __device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int hea
           codes[2 * (b + h) + t] = cvt_e2m1x8(q);
         }
       }
-      sfw[b >> 2] |= (code0 | (code1 << 8)) << (8 * (b & 3));
+      sfb |= static_cast<uint64_t>(code0 | (code1 << 8)) << (8 * b);
     }
-    *reinterpret_cast<uint2*>(args.q_sf + static_cast<long long>(row) * Fp4Layout<kFmt>::kScaleBytesPerToken +
-                              head * 8) = make_uint2(sfw[0], sfw[1]);
   }
+  return sfb;
+}
+
+// FP4 codes, scales and the optional pre-quant output of dims
+// [128 kN/64 * part, +2 kN) of one (token, head), from its Hadamard outputs in
+// p[0..kN): kN = 64 is the whole head (part 0), kN = 32 one half of it.  The
+// codes go to `stage_row`, the (token, head)'s 64 bytes of the shared staging
+// tile, stored with the 64-byte swizzle of the bulk tensor store (16-byte
+// chunk c of row r at chunk c ^ ((r >> 1) & 3)): a warp's 16-byte writes then
+// fall on distinct banks.
+template <int kFmt, int kN>
+__device__ __forceinline__ void fp4_store(const uint64_t* p, int row, int head, int part, const GemmArgs& args,
+                                          uint8_t* stage_row, int swz) {
+  using F = Fp4Layout<kFmt>;
+  constexpr int kBlocks = 2 * kN / F::kBlock;    // scale bytes this call writes
+  uint32_t codes[kN / 4];
+  const uint64_t sfb = fp4_blocks<kFmt, kN>(p, codes);
+  uint8_t* sf = args.q_sf + static_cast<long long>(row) * F::kScaleBytesPerToken + head * F::kBlocksPerHead +
+                part * kBlocks;
+  if constexpr (kBlocks == 8) {
+    *reinterpret_cast<uint2*>(sf) = make_uint2(static_cast<uint32_t>(sfb), static_cast<uint32_t>(sfb >> 32));
+  } else if constexpr (kBlocks == 4) {
+    *reinterpret_cast<uint32_t*>(sf) = static_cast<uint32_t>(sfb);
+  } else {
+    static_assert(kBlocks == 2, "scale bytes per call");
+    *reinterpret_cast<uint16_t*>(sf) = static_cast<uint16_t>(sfb);
+  }
+  constexpr int kChunks = kN / 16;               // 16-byte code chunks
 #pragma unroll
-  for (int t = 0; t < 4; ++t)
-    *reinterpret_cast<uint4*>(stage_row + ((t ^ swz) << 4)) =
+  for (int t = 0; t < kChunks; ++t)
+    *reinterpret_cast<uint4*>(stage_row + (((part * kChunks + t) ^ swz) << 4)) =
         make_uint4(codes[4 * t], codes[4 * t + 1], codes[4 * t + 2], codes[4 * t + 3]);
   if (args.q_pre != nullptr) {
     const uint64_t c2 = f2_pack(kInvSqrt128, kInvSqrt128);
-    float4* pre = reinterpret_cast<float4*>(args.q_pre + static_cast<long long>(row) * kQDim + head * kHeadDim);
+    float4* pre = reinterpret_cast<float4*>(args.q_pre + static_cast<long long>(row) * kQDim + head * kHeadDim +
+                                            part * 2 * kN);
 #pragma unroll
-    for (int t = 0; t < 32; ++t) {
+    for (int t = 0; t < kN / 2; ++t) {
       float z0, z1, z2, z3;
       f2_unpack(f2_mul(p[2 * t], c2), z0, z1);
       f2_unpack(f2_mul(p[2 * t + 1], c2), z2, z3);
       pre[t] = make_float4(z0, z1, z2, z3);
     }
   }
+}
+
+// RoPE, Hadamard, FP4 for one (token, head) in one thread.  p[j] holds dims
+// (2j, 2j+1) of the 128 FP32 GEMM outputs as one packed pair.
+template <int kFmt>
+__device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int head, int pos, const GemmArgs& args,
+                                             uint8_t* stage_row, int swz) {
+  rope_neox64(p, pos, args);
+  fwht_packed<64>(p);
+  fp4_store<kFmt, 64>(p, row, head, 0, args, stage_row, swz);
 }
 
 // kNoLoads: the wait self-test instance.  Its producer issues no TMA loads,
@@ -329,6 +370,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_rope_hadamard_fp4_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ GemmArgs args) {
   static_assert(!kFuse || (kBN == 256 && !kNoLoads), "the fused quantizer runs with two-head tiles");
+  // The next kernel of the stream may be scheduled as soon as every CTA of
+  // this one runs: the quantizer of the next call, for instance, then starts
+  // while this kernel works and waits for its completion before it touches
+  // memory.
+  grid_launch_dependents();
   using L = K2Layout<kBN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -355,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool leader = rank == 0;
   // Epilogue warps that read the accumulator: four per head of the tile (one
   // per 32-lane quarter of tensor memory).
-  constexpr int kDrainWarps = 4 * L::kHeads;
+  constexpr int kDrainWarps = kNumEpiWarps;    // every epilogue warp drains every tile
 
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_x);
@@ -446,6 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   const bool have_tile = my_count > 0;
+  // Set by the epilogue warps once they have arrived on the final cluster
+  // barrier (right after their last accumulator read).
+  bool cluster_arrived = false;
   if (warp == 0) {
     if constexpr (!kNoLoads) {
       if (lane == 0 && have_tile) {
@@ -713,10 +762,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;            // the TMEM lane group this warp may read
-    const int half = (warp - 2) >> 2;     // which head of the tile
-    const bool drains = half < L::kHeads; // warp-uniform: this warp has a head in every tile
+    // Two-head tiles: warps 2-5 take the first head, 6-9 the second.  One-head
+    // tiles: warps w and w + 4 (the same TMEM lanes) share each (token, head),
+    // w the Hadamard outputs 0..63 and w + 4 the outputs 64..127.
+    const int half = (warp - 2) >> 2;
     const int trow = quad * 32 + lane;    // row within the CTA's 128-row tile
-    uint8_t* stage_row = sOut + half * kOutHeadBytes + trow * 64;
+    uint8_t* stage_row = sOut + (L::kHeads == 2 ? half : 0) * kOutHeadBytes + trow * 64;
     const int swz = (trow >> 1) & 3;
     const bool store_issuer = warp == 2 && lane == 0;
     // Fused quantizer.  Wave v of the interleaved order is the run of tiles
@@ -814,21 +865,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       quantize_through(local + 2);
       const int pt = tile_at(local);
       const int row = tile_m0(pt) + trow;
-      const int head = tile_n(pt) * L::kHeads + half;
+      const int head = tile_n(pt) * L::kHeads + (L::kHeads == 2 ? half : 0);
       const int acc = local % L::kAccBufs;
-      const int pos = drains && row < args.M ? static_cast<int>(ld_dependent_u32(args.pos + row)) : 0;   // in flight during the wait
+      const int pos = row < args.M ? static_cast<int>(ld_dependent_u32(args.pos + row)) : 0;   // in flight during the wait
       // The previous tile's bulk stores must have read the staging tile
       // before anyone overwrites it.
       if (store_issuer) tma_store_wait_read();
-      bool got = true;
-      if (drains) {
-        got = mbar_wait(&tmem_full[acc], (local / L::kAccBufs) & 1, timeout);
-        if (!got) fail(abort_flag, kStatusEpilogueWait);
-      }
+      const bool got = mbar_wait(&tmem_full[acc], (local / L::kAccBufs) & 1, timeout);
+      if (!got) fail(abort_flag, kStatusEpilogueWait);
       // One decision for all epilogue warps (they meet at a named barrier
       // below); this barrier also tells them the staging tile is free.
       if (!named_barrier_and(1, kNumEpiWarps * 32, got && *abort_flag == 0u)) break;
-      if (drains) {
+      if constexpr (L::kHeads == 1) {
+        // Sylvester's H_128 = H_2 (x) H_64: the outputs 64 h + i are
+        // H_64(x_0)[i] + (-1)^h H_64(x_1)[i], x_0 = dims 0..63 after RoPE and
+        // x_1 = dims 64..127.  Each warp transforms its own half in place in
+        // tensor memory, the pair meets at a named barrier, and each reads
+        // the other half back: the same operations on every element as in one
+        // thread, so the bytes are the same.
+        tc_fence_after_sync();
+        float v[64];
+        const uint32_t trow_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kAccCol +
+                                   static_cast<uint32_t>(acc * kBN);
+        const uint32_t mine = trow_addr + static_cast<uint32_t>(64 * half);
+        const uint32_t theirs = trow_addr + static_cast<uint32_t>(64 * (half ^ 1));
+        tmem_ld_32x32b_x32(mine, v);
+        tmem_ld_32x32b_x32(mine + 32, v + 32);
+        tmem_ld_wait(v);
+        tmem_ld_wait(v + 32);
+        uint64_t p[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) p[j] = f2_pack(v[2 * j], v[2 * j + 1]);
+        if (half == 0) rope_neox64(p, pos, args);
+        fwht_packed<32>(p);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f2_unpack(p[j], v[2 * j], v[2 * j + 1]);
+        tmem_st_32x32b_x32(mine, v);
+        tmem_st_32x32b_x32(mine + 32, v + 32);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        named_barrier_sync(2 + quad, 64);
+        tc_fence_after_sync();
+        tmem_ld_32x32b_x32(theirs, v);
+        tmem_ld_32x32b_x32(theirs + 32, v + 32);
+        tmem_ld_wait(v);
+        tmem_ld_wait(v + 32);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(tmem_empty_leader0 + 8u * static_cast<uint32_t>(acc));
+        if (!kFuse && local == my_count - 1) {
+          cluster_arrive_release();
+          cluster_arrived = true;
+        }
+        // The last stage (dim bit 6): a + b in the first half, a - b in the
+        // second, a being the first half's values.
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const uint64_t o = f2_pack(v[2 * j], v[2 * j + 1]);
+          p[j] = half == 0 ? f2_add(p[j], o) : f2_sub(o, p[j]);
+        }
+        if (row < args.M) fp4_store<kFmt, 32>(p, row, head, half, args, stage_row, swz);
+      } else {
         tc_fence_after_sync();
         float v[128];
         const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kAccCol +
@@ -847,6 +944,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the leader may overwrite it: a CTA-scope arrive suffices and does not
         // wait for earlier global stores to reach L2.
         if (lane == 0) mbar_arrive_remote(tmem_empty_leader0 + 8u * static_cast<uint32_t>(acc));
+        if (!kFuse && local == my_count - 1) {
+          cluster_arrive_release();
+          cluster_arrived = true;
+        }
         uint64_t p[64];
 #pragma unroll
         for (int j = 0; j < 64; ++j) p[j] = f2_pack(v[2 * j], v[2 * j + 1]);
@@ -870,9 +971,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // Neither CTA leaves (or frees tensor memory) while the pair may still use
-  // its shared memory, barriers or tensor memory.
+  // its shared memory, barriers or tensor memory.  The epilogue warps arrive
+  // as soon as their last accumulator read and remote arrive are done: a
+  // release arrive after the tile's output stores would wait for those to
+  // reach memory (~1 us), and nothing in the other CTA depends on them.
   tc_fence_before_sync();
-  cluster_sync_all();
+  if (!cluster_arrived) cluster_arrive_release();
+  cluster_wait();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc_pair(tmem, kTmemCols);

@@ -53,8 +53,12 @@ __global__ void __launch_bounds__(kThreads) quant_1x128_kernel(const uint16_t* _
                                                                long long ldy, int32_t* __restrict__ sf, int m_al,
                                                                int groups) {
   // The fused GEMM that usually follows may be scheduled now; it waits for
-  // this grid's completion before reading anything.
+  // this grid's completion before reading anything.  This kernel is itself
+  // launched as a programmatic dependent of whatever precedes it in the
+  // stream, so its blocks may be resident before that kernel ends: nothing
+  // is read or written before the dependency wait.
   grid_launch_dependents();
+  grid_dependency_wait();
   const long long unit = (static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (unit >= static_cast<long long>(m_al) * groups) return;
@@ -176,9 +180,18 @@ cudaError_t launch_quant_1x128(const void* x, int M, int K, long long ldx, void*
   const int groups = (K + 511) / 512;
   const long long warps = static_cast<long long>(m_al) * groups;
   const long long blocks = (warps * 32 + kThreads - 1) / kThreads;
-  quant_1x128_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(x), M, K, ldx, static_cast<uint8_t*>(y), ldy, sf, m_al, groups);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quant_1x128_kernel, static_cast<const uint16_t*>(x), M, K, ldx,
+                            static_cast<uint8_t*>(y), ldy, sf, m_al, groups);
 }
 
 cudaError_t launch_quant_1x128_host_rows(const void* x, int M, int K, long long ldx, void* y, long long ldy,
