@@ -205,8 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t acc_empty_l0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
   const int pair_id = static_cast<int>(cluster_id_x());
   const int num_pairs = static_cast<int>(cluster_count_x());
-  // The queries' FP4 Q may be the preceding kernel's output.
+  // The queries' FP4 Q may be the preceding kernel's output.  The next
+  // kernel (the top-k selection) may be scheduled now: it waits for this
+  // one's completion before it reads the scores.
   grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
