@@ -174,7 +174,10 @@ size_t iq_fp8_scale_words(int M, int K);
  * Requirements: M >= 0; K > 0 and K % 128 == 0 (else IQ_ERR_SHAPE);
  *   ldx >= K, ldy >= K; x and y 16-byte aligned, ldx % 8 == 0 and
  *   ldy % 16 == 0, scales 4-byte aligned (else IQ_ERR_ALIGN).
- * M == 0 returns IQ_OK without a launch.  One kernel launch. */
+ * M == 0 returns IQ_OK without a launch.  One kernel launch, with programmatic
+ * stream serialization: its blocks may be scheduled while the preceding
+ * kernel on `stream` runs, and they touch no memory before that kernel has
+ * completed. */
 iq_status iq_fp8_quant_1x128_ue8m0(const void* x_bf16, int M, int K, int ldx,
                                    void* y_e4m3, int ldy, int32_t* scales,
                                    cudaStream_t stream);
@@ -238,14 +241,21 @@ size_t iq_prepare_q_workspace(int M);
  * that quantized its rows; that launch is cooperative (all of its CTAs, one
  * per SM, resident at once).
  *
- * Ordering: the small-M GEMM kernel reads wq_e4m3 and wq_sf before the kernel
- * launched just before it on `stream` has completed (that kernel is the
- * quantizer for iq_prepare_q; for iq_gemm_rope_hadamard_fp4 it is whatever
- * the caller launched last, and the overlap happens only if that kernel
- * allows programmatic dependents).  The weights must therefore not be written
- * by the immediately preceding kernel.  Every other input is read after that
- * kernel has completed.  Calls that run at the same time must not share a
- * workspace. */
+ * Ordering: the GEMM kernels of both routes read wq_e4m3 and wq_sf before the
+ * kernel launched just before them on `stream` has completed (that kernel is
+ * the quantizer for iq_prepare_q; for iq_gemm_rope_hadamard_fp4 it is
+ * whatever the caller launched last, and the overlap happens only if that
+ * kernel allows programmatic dependents).  The weights must therefore not be
+ * written by the immediately preceding kernel.  Every other input is read
+ * after that kernel has completed; the quantizer, itself launched as a
+ * programmatic dependent of whatever precedes it, touches no memory before
+ * that.  The kernels let the next kernel on `stream` be scheduled while they
+ * run (griddepcontrol.launch_dependents): a following kernel launched with
+ * programmatic stream serialization must wait for them
+ * (griddepcontrol.wait) before it reads this call's outputs or workspace, as
+ * that launch mode requires of any kernel.  Calls that run at the same time
+ * must not share a workspace; calls enqueued one after another on one stream
+ * may. */
 iq_status iq_prepare_q(const void* latent_bf16, int M,
                        const void* wq_e4m3, const uint8_t* wq_sf,
                        const int32_t* positions,
