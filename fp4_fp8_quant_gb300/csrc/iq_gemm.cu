@@ -17,8 +17,9 @@
 // GB300 the 1-SM M = 128 MMA measured 1.3-1.6x slower per SM than this form,
 // which reaches the tensor-core peak.  K = 1536 streams as twelve 128-byte
 // K-blocks.  Each pair takes a contiguous run of tiles, by default in
-// token-major order (consecutive tiles share their token rows); a one-head
-// tile width (128 features) is kept as an instance for measurements.
+// token-major order (consecutive tiles share their token rows).  Up to 256
+// tokens the tile is one head wide (128 features, each CTA loading 64 W rows
+// of the head), so that twice as many pairs share the work.
 // Warp roles (320 threads per CTA):
 //   warp 0      TMA producer (both CTAs): a 6-stage ring of {X 16 KB, W 16 KB},
 //               128-byte swizzled; each load signals the leader CTA's barrier.
