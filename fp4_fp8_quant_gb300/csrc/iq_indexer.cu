@@ -129,7 +129,7 @@ __device__ __forceinline__ int chunk_lengths(const IndexerArgs& a, int ch, int l
   const int kb = ch / a.chunks_per_block;
   const int t = (ch - kb * a.chunks_per_block) * kChunkTokens + lane;
   if (t >= a.M) return 0;
-  const int L = __ldg(a.len + t);
+  const int L = static_cast<int>(ld_dependent_u32(a.len + t));
   return L < 0 ? 0 : (L > a.N ? a.N : L);
 }
 
@@ -144,12 +144,15 @@ __device__ __forceinline__ void store_scale_rows(uint32_t* dst, int lane, const 
 }
 
 // Four consecutive scale words from `src`, of which the first `n` exist.
+// The query scales are the preceding kernel's output, so these are loads that
+// stay below the dependency wait (not the read-only path, which the compiler
+// may hoist above it).
 __device__ __forceinline__ uint4 load_scale_words(const uint32_t* src, int n) {
-  if (n >= 4) return __ldg(reinterpret_cast<const uint4*>(src));
+  if (n >= 4) return ld_dependent_v4(src);
   uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  if (n > 0) v.x = __ldg(src);
-  if (n > 1) v.y = __ldg(src + 1);
-  if (n > 2) v.z = __ldg(src + 2);
+  if (n > 0) v.x = ld_dependent_u32(src);
+  if (n > 1) v.y = ld_dependent_u32(src + 1);
+  if (n > 2) v.z = ld_dependent_u32(src + 2);
   return v;
 }
 
@@ -542,12 +545,14 @@ __device__ uint32_t find_digit(const uint32_t* hist, int nb, uint32_t rank, uint
 // global memory once, as order-preserving keys into shared memory; longer
 // rows are read again by every pass.
 __global__ void __launch_bounds__(kTopkThreads)
-    indexer_topk_kernel(const float* __restrict__ logits, long long ld, int N, const int32_t* __restrict__ len,
-                        int k, int32_t* __restrict__ out, int cache_keys) {
+    indexer_topk_kernel(const float* logits, long long ld, int N, const int32_t* len, int k,
+                        int32_t* __restrict__ out, int cache_keys) {
   extern __shared__ uint32_t cache[];   // cache_keys words
   __shared__ uint32_t hist[2048];
   __shared__ uint32_t scratch[kTopkThreads / 32];
-  // The scores are the preceding kernel's output.
+  // The scores are the preceding kernel's output.  They and the lengths are
+  // read through plain pointers (no __restrict__, no read-only path), so the
+  // compiler keeps those loads below the wait.
   grid_dependency_wait();
   const int t = blockIdx.x;
   const float* row = logits + static_cast<long long>(t) * ld;

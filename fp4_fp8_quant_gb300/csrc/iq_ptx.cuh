@@ -161,6 +161,16 @@ __device__ __forceinline__ uint32_t ld_dependent_u32(const void* p) {
   return v;
 }
 
+// 128-bit form of ld_dependent_u32 (16-byte aligned address).
+__device__ __forceinline__ uint4 ld_dependent_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(reinterpret_cast<uint64_t>(p))
+               : "memory");
+  return v;
+}
+
 // 64-bit load with acquire semantics at GPU scope: later memory accesses of
 // this thread see what the releasing writer wrote before its release.
 __device__ __forceinline__ uint64_t ld_acquire_u64(const void* p) {

@@ -5,7 +5,10 @@ memory access.  Calls issued without a host synchronisation between them, on
 one shared workspace, must therefore give the bytes each call gives alone,
 and a quantizer whose input the immediately preceding kernel writes must read
 the new values (TensorRT-LLM PR "Fuse DeepSeek-V4 Indexer Q projection with
-CuTe DSL", sequence diagram: the quantization, then the GEMM on its output)."""
+CuTe DSL", sequence diagram: the quantization, then the GEMM on its output);
+the same holds for the indexer kernels that consume the prepared Q (TokenSpeed
+PR "perf(deepseek-v4): accelerate indexer Q and packed FP8 quantization",
+Summary)."""
 
 import numpy as np
 import pytest
@@ -107,3 +110,42 @@ def test_stand_alone_quantizer_after_a_writer(cuda_device):
     torch.cuda.synchronize()
     for (y, s), (yw, sw) in zip(got, want):
         assert torch.equal(y, yw) and torch.equal(s, sw)
+
+
+def test_prepare_then_indexer_without_synchronisation(cuda_device):
+    """prepare_q -> indexer_logits -> indexer_topk, three times in a row on one
+    stream with new latents and shared buffers: the logits kernel reads the
+    FP4 Q and its scales that the GEMM just wrote, the top-k reads the scores
+    the logits kernel just wrote (each waits for its predecessor while both
+    may be resident), and every result must equal the same calls made one at
+    a time with synchronisations between them."""
+    iq = _iq()
+    M, N = 2000, 3000
+    lats, w, ws, p = _inputs(M, 3, 700)
+    k_np, ks_np = W.indexer_keys(N, seed=5)
+    kf, ksf = torch.from_numpy(k_np).cuda(), torch.from_numpy(ks_np).cuda()
+    hw = torch.from_numpy(W.indexer_weights(M, seed=6)).cuda()
+    lengths = torch.from_numpy(np.clip(np.arange(N - M, N) + 1, 0, N).astype(np.int32)).cuda()
+    want = []
+    for lat in lats:
+        q, s = _alone(iq, lat, w, ws, p)
+        lg = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+        iq.indexer_logits(q, s, kf, ksf, hw, lengths, logits=lg)
+        torch.cuda.synchronize()
+        top = iq.indexer_topk(lg, lengths, 1024)
+        torch.cuda.synchronize()
+        want.append((lg.clone(), top.clone()))
+    q = torch.empty((M, 4096), dtype=torch.uint8, device="cuda")
+    s = torch.empty((M, 256), dtype=torch.uint8, device="cuda")
+    work = torch.empty(iq.prepare_q_workspace_bytes(M), dtype=torch.uint8, device="cuda")
+    lg = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    got = []
+    for lat in lats:
+        iq.prepare_q(lat, w, ws, p, q_fp4=q, q_sf=s, workspace=work)
+        iq.indexer_logits(q, s, kf, ksf, hw, lengths, logits=lg)
+        top = iq.indexer_topk(lg, lengths, 1024)
+        got.append((lg.clone(), top))
+    torch.cuda.synchronize()
+    for (lg_g, top_g), (lg_w, top_w) in zip(got, want):
+        assert torch.equal(lg_g, lg_w) and torch.equal(top_g, top_w)
+    assert iq.device_status() == 0
