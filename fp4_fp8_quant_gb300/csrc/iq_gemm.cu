@@ -89,6 +89,9 @@ constexpr uint32_t kAccCol = 0;                  // accumulators: columns 0..255
 constexpr uint32_t kSfaCol = 256;
 constexpr uint32_t kSfbCol = 320;
 constexpr uint32_t kSfBufCols = 32;
+// Two-head tiles: the RoPE rotation's cos/sin of each CTA row, per head of the
+// tile (64 columns each), reused by the next tiles on the same token rows.
+constexpr uint32_t kRopeCol = kSfbCol + 2 * kSfBufCols;
 constexpr int kSfaWords = kScaleGroups * 128;    // per buffer
 constexpr int kOutHeadBytes = BM * 64;           // FP4 codes of one head of the CTA's rows
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1;
@@ -120,6 +123,7 @@ struct K2Layout {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kAccBufs * kBN <= static_cast<int>(kSfaCol), "accumulators below the scale columns");
   static_assert(kSfbCol + 2 * kSfBufCols <= kTmemCols && kSfaCol + 2 * kSfBufCols <= kSfbCol, "scale columns");
+  static_assert(kBN == 128 || kRopeCol + 64 * kHeads <= kTmemCols, "cos/sin columns");
 };
 
 __device__ __forceinline__ void fail(volatile uint32_t* abort_flag, uint32_t bit) {
@@ -205,6 +209,53 @@ __device__ __forceinline__ void rope_neox64(uint64_t* p, int pos, const GemmArgs
     const uint64_t x1 = p[i >> 1], x2 = p[(i >> 1) + 16];
     p[i >> 1] = f2_fma(x1, c, f2_mul(x2, f2_neg(s)));        // x1 c - x2 s
     p[(i >> 1) + 16] = f2_fma(x2, c, f2_mul(x1, s));         // x2 c + x1 s
+  }
+}
+
+// The RoPE rotation's cos/sin of one row kept in tensor memory at column
+// taddr (this warp's lanes): frequency pair j = (2j, 2j+1) at columns
+// 4j..4j+3 as (cos, cos, sin, sin), computed as rope_neox64 computes them.
+// Warp-collective: every lane of the warp takes part.
+__device__ __forceinline__ void rope_cs_fill(int pos, const GemmArgs& args, uint32_t taddr) {
+  const float pf = static_cast<float>(pos);
+  const uint64_t pp = f2_pack(pf, pf);
+  const uint64_t shift = f2_pack(12582912.0f, 12582912.0f);
+  const uint64_t two_pi = f2_pack(kTwoPi, kTwoPi);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const uint64_t hi = f2_pack(args.rope.hi[i], args.rope.hi[i + 1]);
+    const uint64_t lo = f2_pack(args.rope.lo[i], args.rope.lo[i + 1]);
+    const uint64_t th = f2_mul(pp, hi);
+    uint64_t tl = f2_fma(pp, hi, f2_neg(th));
+    tl = f2_fma(pp, lo, tl);
+    const uint64_t rn = f2_sub(f2_add(th, shift), shift);
+    const uint64_t ang = f2_mul(f2_add(f2_sub(th, rn), tl), two_pi);
+    float a0, a1, s0, c0, s1, c1;
+    f2_unpack(ang, a0, a1);
+    __sincosf(a0, &s0, &c0);
+    __sincosf(a1, &s1, &c1);
+    tmem_st_32x32b_x4(taddr + 2u * static_cast<uint32_t>(i), c0, c1, s0, s1);
+  }
+  tmem_st_wait();
+}
+
+// RoPE on p[0..31] (as rope_neox64) with the cos/sin that rope_cs_fill
+// stored: the same floats, so the same results.  Warp-collective.
+__device__ __forceinline__ void rope_apply_cached(uint64_t* p, uint32_t taddr) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float v[16];
+    tmem_ld_32x32b_x16(taddr + 16u * static_cast<uint32_t>(q), v);
+    tmem_ld_wait16(v);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int i = 2 * (4 * q + jj);
+      const uint64_t c = f2_pack(v[4 * jj], v[4 * jj + 1]);
+      const uint64_t s = f2_pack(v[4 * jj + 2], v[4 * jj + 3]);
+      const uint64_t x1 = p[i >> 1], x2 = p[(i >> 1) + 16];
+      p[i >> 1] = f2_fma(x1, c, f2_mul(x2, f2_neg(s)));        // x1 c - x2 s
+      p[(i >> 1) + 16] = f2_fma(x2, c, f2_mul(x1, s));         // x2 c + x1 s
+    }
   }
 }
 
@@ -348,16 +399,6 @@ __device__ __forceinline__ void fp4_store(const uint64_t* p, int row, int head, 
       pre[t] = make_float4(z0, z1, z2, z3);
     }
   }
-}
-
-// RoPE, Hadamard, FP4 for one (token, head) in one thread.  p[j] holds dims
-// (2j, 2j+1) of the 128 FP32 GEMM outputs as one packed pair.
-template <int kFmt>
-__device__ __forceinline__ void epilogue_row(uint64_t (&p)[64], int row, int head, int pos, const GemmArgs& args,
-                                             uint8_t* stage_row, int swz) {
-  rope_neox64(p, pos, args);
-  fwht_packed<64>(p);
-  fp4_store<kFmt, 64>(p, row, head, 0, args, stage_row, swz);
 }
 
 // kNoLoads: the wait self-test instance.  Its producer issues no TMA loads,
@@ -862,13 +903,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_wave(q_next);
       }
     };
+    int rope_mp = -1;   // the row block whose cos/sin are in tensor memory
     for (int local = 0; local < my_count; ++local) {
       quantize_through(local + 2);
       const int pt = tile_at(local);
+      const bool rope_cached = tile_mp(pt) == rope_mp;   // warp-uniform
+      rope_mp = tile_mp(pt);
       const int row = tile_m0(pt) + trow;
       const int head = tile_n(pt) * L::kHeads + (L::kHeads == 2 ? half : 0);
       const int acc = local % L::kAccBufs;
       const int pos = row < args.M ? static_cast<int>(ld_dependent_u32(args.pos + row)) : 0;   // in flight during the wait
+      // Two-head tiles: the rotation's cos/sin depend on the row alone, so
+      // they are computed (while the tile's MMAs run) only on a pair's first
+      // tile of a row block and read back from tensor memory afterwards.
+      const uint32_t rope_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kRopeCol +
+                                 static_cast<uint32_t>(64 * half);
+      if constexpr (L::kHeads == 2) {
+        if (!rope_cached) rope_cs_fill(pos, args, rope_addr);
+      }
       // The previous tile's bulk stores must have read the staging tile
       // before anyone overwrites it.
       if (store_issuer) tma_store_wait_read();
@@ -948,7 +1000,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t p[64];
 #pragma unroll
         for (int j = 0; j < 64; ++j) p[j] = f2_pack(v[2 * j], v[2 * j + 1]);
-        if (row < args.M) epilogue_row<kFmt>(p, row, head, pos, args, stage_row, swz);
+        rope_apply_cached(p, rope_addr);
+        fwht_packed<64>(p);
+        if (row < args.M) fp4_store<kFmt, 64>(p, row, head, 0, args, stage_row, swz);
       }
       fence_proxy_async_smem();
       named_barrier_sync(1, kNumEpiWarps * 32);
