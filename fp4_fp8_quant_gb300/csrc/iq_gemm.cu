@@ -179,43 +179,17 @@ __device__ __forceinline__ int unit_owner(long long u, long long units, int G) {
   return static_cast<int>(((u + 1) * G - 1) / units);
 }
 
-// NeoX RoPE on dims 0..63 of a (token, head), held as p[0..31] (p[j] = dims
-// 2j, 2j+1 as one packed pair): pairs (i, i+32), angle = pos * 10000^(-i/32).
-// The angle is reduced in turns with a two-float product (head and tail of
-// the frequency, exact FMA residue) so that it stays accurate for large
-// positions; the reduced angle lies in [-pi, pi].  Frequencies i and i+1 go
-// through the packed lanes together; rounding to an integer uses the
-// 1.5 * 2^23 shift, exact for |turns| < 2^22.
-__device__ __forceinline__ void rope_neox64(uint64_t* p, int pos, const GemmArgs& args) {
-  const float pf = static_cast<float>(pos);
-  const uint64_t pp = f2_pack(pf, pf);
-  const uint64_t shift = f2_pack(12582912.0f, 12582912.0f);
-  const uint64_t two_pi = f2_pack(kTwoPi, kTwoPi);
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    const uint64_t hi = f2_pack(args.rope.hi[i], args.rope.hi[i + 1]);
-    const uint64_t lo = f2_pack(args.rope.lo[i], args.rope.lo[i + 1]);
-    const uint64_t th = f2_mul(pp, hi);
-    uint64_t tl = f2_fma(pp, hi, f2_neg(th));
-    tl = f2_fma(pp, lo, tl);
-    const uint64_t rn = f2_sub(f2_add(th, shift), shift);
-    const uint64_t ang = f2_mul(f2_add(f2_sub(th, rn), tl), two_pi);
-    float a0, a1, s0, c0, s1, c1;
-    f2_unpack(ang, a0, a1);
-    __sincosf(a0, &s0, &c0);
-    __sincosf(a1, &s1, &c1);
-    const uint64_t c = f2_pack(c0, c1);
-    const uint64_t s = f2_pack(s0, s1);
-    const uint64_t x1 = p[i >> 1], x2 = p[(i >> 1) + 16];
-    p[i >> 1] = f2_fma(x1, c, f2_mul(x2, f2_neg(s)));        // x1 c - x2 s
-    p[(i >> 1) + 16] = f2_fma(x2, c, f2_mul(x1, s));         // x2 c + x1 s
-  }
-}
-
-// The RoPE rotation's cos/sin of one row kept in tensor memory at column
-// taddr (this warp's lanes): frequency pair j = (2j, 2j+1) at columns
-// 4j..4j+3 as (cos, cos, sin, sin), computed as rope_neox64 computes them.
-// Warp-collective: every lane of the warp takes part.
+// NeoX RoPE on dims 0..63 of a (token, head): pairs (i, i+32), angle = pos *
+// 10000^(-i/32).  The angle is reduced in turns with a two-float product
+// (head and tail of the frequency, exact FMA residue) so that it stays
+// accurate for large positions; the reduced angle lies in [-pi, pi].
+// Frequencies i and i+1 go through the packed lanes together; rounding to an
+// integer uses the 1.5 * 2^23 shift, exact for |turns| < 2^22.
+//
+// rope_cs_fill computes one row's cos/sin and keeps them in tensor memory at
+// column taddr (this warp's lanes): frequency pair j = (2j, 2j+1) at columns
+// 4j..4j+3 as (cos, cos, sin, sin).  Warp-collective: every lane of the warp
+// takes part.
 __device__ __forceinline__ void rope_cs_fill(int pos, const GemmArgs& args, uint32_t taddr) {
   const float pf = static_cast<float>(pos);
   const uint64_t pp = f2_pack(pf, pf);
@@ -239,8 +213,8 @@ __device__ __forceinline__ void rope_cs_fill(int pos, const GemmArgs& args, uint
   tmem_st_wait();
 }
 
-// RoPE on p[0..31] (as rope_neox64) with the cos/sin that rope_cs_fill
-// stored: the same floats, so the same results.  Warp-collective.
+// RoPE on p[0..31] (p[j] = dims 2j, 2j+1 as one packed pair) with the
+// cos/sin that rope_cs_fill stored.  Warp-collective.
 __device__ __forceinline__ void rope_apply_cached(uint64_t* p, uint32_t taddr) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -913,14 +887,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int head = tile_n(pt) * L::kHeads + (L::kHeads == 2 ? half : 0);
       const int acc = local % L::kAccBufs;
       const int pos = row < args.M ? static_cast<int>(ld_dependent_u32(args.pos + row)) : 0;   // in flight during the wait
-      // Two-head tiles: the rotation's cos/sin depend on the row alone, so
-      // they are computed (while the tile's MMAs run) only on a pair's first
-      // tile of a row block and read back from tensor memory afterwards.
+      // The rotation's cos/sin depend on the row alone, so they are computed
+      // while the tile's MMAs run (before the accumulator wait), only on a
+      // pair's first tile of a row block, and read back from tensor memory
+      // (one-head tiles: by the warps of dims 0..63 alone).
       const uint32_t rope_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kRopeCol +
-                                 static_cast<uint32_t>(64 * half);
-      if constexpr (L::kHeads == 2) {
-        if (!rope_cached) rope_cs_fill(pos, args, rope_addr);
-      }
+                                 static_cast<uint32_t>(L::kHeads == 2 ? 64 * half : 0);
+      const bool rope_warp = L::kHeads == 2 || half == 0;   // warp-uniform
+      if (rope_warp && !rope_cached) rope_cs_fill(pos, args, rope_addr);
       // The previous tile's bulk stores must have read the staging tile
       // before anyone overwrites it.
       if (store_issuer) tma_store_wait_read();
@@ -949,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t p[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) p[j] = f2_pack(v[2 * j], v[2 * j + 1]);
-        if (half == 0) rope_neox64(p, pos, args);
+        if (half == 0) rope_apply_cached(p, rope_addr);
         fwht_packed<32>(p);
 #pragma unroll
         for (int j = 0; j < 32; ++j) f2_unpack(p[j], v[2 * j], v[2 * j + 1]);
