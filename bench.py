@@ -9,8 +9,10 @@ synthetic data resident in HBM before the timed region; L2 is flushed (256 MB
 written, then 256 MB read, so no dirty lines are left for the timed kernels to
 write back) between timed steps, outside the CUDA-event intervals.  `value` is
 the token count over the median of the K event-timed steps (mean, minimum and
-maximum are reported beside it); the warm-up runs at least W steps and at
-least half a second.  The steady state of steps run back to back over
+maximum are reported beside it); the clock sampler starts first, the GPU
+idles for a second, and the warm-up runs max(3, W) steps (longer warm-ups
+leave GB300 in its power-capped state for the first timed steps).  The steady
+state of steps run back to back over
 rotating buffer sets (total over twice the L2 size; each step then also
 writes back the outputs of earlier steps) is reported as `back_to_back`.  Also measured in the same run: the quantizer alone on
 BF16 [4632, 7168] (GB/s against HBM), the GEMM's own launch time (for the
@@ -51,7 +53,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0            # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 ORACLE_SAMPLE_ROWS = 4632      # rows of the prefill workload per oracle timing (all of it)
-WARMUP_MIN_S = 0.5             # the warm-up also lasts at least this long (clocks leave idle)
+SETTLE_S = 1.0                 # idle time between the clock sampler's first sample and the warm-up
 NOMINAL_HBM_GBS = 7900.0       # HBM3e nominal bandwidth of GB300
 NOMINAL_FP8_TFLOPS = 4500.0    # dense FP8 tensor nominal of GB300
 
@@ -380,17 +382,19 @@ def run_ours(args):
                                     q_sf=c["s"] if s is None else s, workspace=c["work"], fp4_format=fmt)
 
     steps = [step_fn(c) for c in chain_sets]
-    # The clock sampler starts before the warm-up, so its start-up and the
-    # clocks' ramp from idle both fall before the timed steps.  The warm-up is
-    # at least W steps and at least WARMUP_MIN_S of them.
+    # The clock sampler starts before the warm-up and the GPU then idles for
+    # SETTLE_S, so that the sampler's start-up falls outside the timed steps
+    # and the timed steps start from the state the sweep's points start from.
+    # The warm-up is max(3, W) steps: on GB300 a longer one (0.1 s or more of
+    # back-to-back steps) leaves the GPU in its power-capped state for the
+    # next few hundred ms, where a flushed step takes ~10 % longer; sustained
+    # load is what `back_to_back` reports.
     clocks = ClockSampler(local).__enter__()
-    t0 = time.perf_counter()
+    time.sleep(SETTLE_S)
     n_warm = 0
-    while n_warm < max(3, args.warmup) or time.perf_counter() - t0 < WARMUP_MIN_S:
+    while n_warm < max(3, args.warmup):
         steps[n_warm % n_sets]()
         n_warm += 1
-        if n_warm % 64 == 0:
-            torch.cuda.synchronize()
     # Timed steps: each after an L2 flush (256 MB written, then 256 MB read,
     # so that no dirty lines of earlier work are left for the step to write
     # back), outside the event interval; the GPU is idle when the step is
@@ -445,6 +449,7 @@ def run_ours(args):
         c = chain_sets[i % n_sets]
         iq.gemm_rope_hadamard_fp4(c["xq"], c["xs"], c["w"], ws, c["p"], q_fp4=c["q"], q_sf=c["s"])
 
+    time.sleep(SETTLE_S)   # out of the power-capped state the back-to-back steps leave
     k2_ms = flushed_ms(k1_of, k2_of, args.steps)
     k2_avg_ms = sum(k2_ms) / len(k2_ms)
     k1_ms = flushed_ms(None, k1_of, args.steps)
