@@ -74,6 +74,21 @@ def test_sweep_points_sampled_rows(cuda_device, M):
     assert sf.min() >= 112 and sf.max() < 160
 
 
+@pytest.mark.parametrize("M", [4633, 4864, 4865])
+def test_prefill_tails_sampled_rows(cuda_device, M):
+    """Token counts around the prefill size: one row past 4632 (a twentieth
+    256-row block with one row), exactly 19 blocks, and one row past that.
+    Sampled rows include every 128-row tile edge of the last two blocks."""
+    x, wq, wsf, pos = W.chain_workload(M, seed=M, outlier_p=0.001, outlier_scale=50.0)
+    q, sf, z = _run(x, wq, wsf, pos)
+    rng = np.random.default_rng(M)
+    edges = [e for b in range(4352, M + 1, 128) for e in (b - 1, b) if e < M]
+    rows = np.unique(np.concatenate([rng.choice(M, 48, replace=False), edges, [0, M - 1]]))
+    oq, osf, oz = O.prequant_q_rows(x, wq, wsf, pos, rows)
+    check_prequant(z[rows], oz)
+    check_fp4(q[rows], sf[rows], oq, osf, oz)
+
+
 def test_nondebug_equals_debug_and_stage_two_alone(cuda_device):
     iq = _iq()
     x, wq, wsf, pos = W.chain_workload(777, seed=9, outlier_p=0.005, outlier_scale=100.0)
