@@ -76,7 +76,7 @@ constexpr int kKbPerCta = kNumKBlocks / kSplit;     // 6
 constexpr int kWBytes = kHeadDim * 128;             // one head x one K-block: 16 KB
 constexpr int kXBytes = kN * 128;                   // 64 tokens x one K-block: 8 KB
 constexpr int kSlots = kN / kSplit;                 // tokens finished per CTA
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTokPerWarp = kSlots / kWarps;        // tokens a warp finishes in step (3)
 // MMA issuers (see above): issuer q takes K-blocks q, q + kIssuers, ... into
@@ -321,27 +321,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // (1) This CTA's partial sums over its K half: TMEM lane d = dim d of the
   // head, column j of accumulator q = token j.  Warp w reads lanes
-  // 32 (w % 4).. and tokens 32 (w / 4)..
+  // 32 (w % 4).. and tokens 16 (w / 4)..
   const bool got = mbar_wait(mma_done, 0, timeout);
   if (!got) fail(abort_flag, kStatusEpilogueWait);
   __syncwarp();   // the lanes left the polling loop separately; tcgen05.ld is .sync.aligned
   tc_fence_after_sync();
   const int quad = warp & 3;
-  const int col0 = (warp >> 2) * 32;
+  constexpr int kCols = kN / (kWarps / 4);   // tokens per warp in steps (1) and (2)
+  static_assert(kCols == 16, "16-column tensor-memory loads");
+  const int col0 = (warp >> 2) * kCols;
   const int d = quad * 32 + lane;
-  float v[32];
+  float v[kCols];
   const bool have = col0 < M;   // warp-uniform
   if (have) {
     const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kAccCol + static_cast<uint32_t>(col0);
-    tmem_ld_32x32b_x32(taddr, v);
-    tmem_ld_wait(v);
+    tmem_ld_32x32b_x16(taddr, v);
+    tmem_ld_wait16(v);
 #pragma unroll
     for (int q = 1; q < kIssuers; ++q) {
-      float u[32];
-      tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(q * kN), u);
-      tmem_ld_wait(u);
+      float u[kCols];
+      tmem_ld_32x32b_x16(taddr + static_cast<uint32_t>(q * kN), u);
+      tmem_ld_wait16(u);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] += u[j];
+      for (int j = 0; j < kCols; ++j) v[j] += u[j];
     }
   }
   tc_fence_before_sync();
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_to[2] = {mapa_shared(smem_u32(red_full), 0), mapa_shared(smem_u32(red_full), 1)};
   if (have) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < kCols; ++j) {
       const int t = col0 + j;   // col0 is even: t % 2 == j % 2
       if (t < M)
         st_async_cluster_f32(red_to[j & 1] + static_cast<uint32_t>((t >> 1) * kHeadDim * 4), v[j], bar_to[j & 1]);
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // (3) Per token one warp: lane l holds dims 4l..4l+3 of the head.  A warp
-  // takes its kTokPerWarp tokens (slots warp, warp + 8, ...) together, so the
+  // takes its kTokPerWarp tokens (slots warp, warp + kWarps, ...) together, so the
   // shuffle and sincos latencies of one token overlap those of the others.
   float x[kTokPerWarp][4];
 #pragma unroll
