@@ -39,7 +39,7 @@
 //     lowest Hadamard stages run in registers and the five others across
 //     lanes with shuffles, each FP4 block of 32 dims is 8 lanes, and every
 //     lane writes its 2 code bytes, so a warp stores the head's 64 code bytes
-//     of the token at once.  A warp takes its four tokens together, so their
+//     of the token at once.  A warp takes its two tokens together, so their
 //     shuffle and sincos latencies overlap.
 //
 // Scale factors, as in the large-M kernel: the MMA applies one UE8M0 scale
