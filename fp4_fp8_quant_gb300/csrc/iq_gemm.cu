@@ -260,10 +260,12 @@ __device__ __forceinline__ void fwht_packed(uint64_t* p) {
 }
 
 // FP4 of z = v / sqrt(128) for the 2 kN Hadamard outputs in p[0..kN), whole
-// blocks of the variant: codes[w] holds dims 8w..8w+7 as E2M1 nibbles, and
-// byte b of the result is block b's scale.
-template <int kFmt, int kN>
-__device__ __forceinline__ uint64_t fp4_blocks(const uint64_t* p, uint32_t* codes) {
+// blocks of the variant.  The codes of dims 32t..32t+31 (four words, word w
+// = dims 8w..8w+7 as E2M1 nibbles) go to chunk(t, words) as soon as they are
+// formed, so that few code registers are live; byte b of the result is block
+// b's scale.
+template <int kFmt, int kN, typename Chunk>
+__device__ __forceinline__ uint64_t fp4_blocks(const uint64_t* p, Chunk&& chunk) {
   uint64_t sfb = 0;
   if constexpr (kFmt != kFp4Nv) {
     // MXFP4: per 32-block UE8M0 exponent e; codes = E2M1(z * 2^-e), formed
@@ -280,13 +282,15 @@ __device__ __forceinline__ uint64_t fp4_blocks(const uint64_t* p, uint32_t* code
       const int e = fp4_block_exponent<kFmt>(amax * kInvSqrt128);
       const float k = fp4_code_factor(e);
       const uint64_t kk = f2_pack(k, k);
+      uint32_t codes[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         float q[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) f2_unpack(f2_mul(p[16 * b + 4 * t + j], kk), q[2 * j], q[2 * j + 1]);
-        codes[4 * b + t] = cvt_e2m1x8(q);
+        codes[t] = cvt_e2m1x8(q);
       }
+      chunk(b, codes);
       sfb |= static_cast<uint64_t>(e + 127) << (8 * b);
     }
   } else {
@@ -314,6 +318,7 @@ __device__ __forceinline__ uint64_t fp4_blocks(const uint64_t* p, uint32_t* code
       const uint32_t code0 = nvfp4_code(t0), code1 = nvfp4_code(t1);
       float k0, k1;
       f2_unpack(f2_mul(f2_pack(e4m3_reciprocal(code0), e4m3_reciprocal(code1)), c2), k0, k1);
+      uint32_t codes[4];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const float kh = h == 0 ? k0 : k1;
@@ -323,9 +328,10 @@ __device__ __forceinline__ uint64_t fp4_blocks(const uint64_t* p, uint32_t* code
           float q[8];
 #pragma unroll
           for (int j = 0; j < 4; ++j) f2_unpack(f2_mul(p[8 * (b + h) + 4 * t + j], kk), q[2 * j], q[2 * j + 1]);
-          codes[2 * (b + h) + t] = cvt_e2m1x8(q);
+          codes[2 * h + t] = cvt_e2m1x8(q);
         }
       }
+      chunk(b / 2, codes);
       sfb |= static_cast<uint64_t>(code0 | (code1 << 8)) << (8 * b);
     }
   }
@@ -344,8 +350,10 @@ __device__ __forceinline__ void fp4_store(const uint64_t* p, int row, int head, 
                                           uint8_t* stage_row, int swz) {
   using F = Fp4Layout<kFmt>;
   constexpr int kBlocks = 2 * kN / F::kBlock;    // scale bytes this call writes
-  uint32_t codes[kN / 4];
-  const uint64_t sfb = fp4_blocks<kFmt, kN>(p, codes);
+  constexpr int kChunks = kN / 16;               // 16-byte code chunks
+  const uint64_t sfb = fp4_blocks<kFmt, kN>(p, [&](int t, const uint32_t (&c)[4]) {
+    *reinterpret_cast<uint4*>(stage_row + (((part * kChunks + t) ^ swz) << 4)) = make_uint4(c[0], c[1], c[2], c[3]);
+  });
   uint8_t* sf = args.q_sf + static_cast<long long>(row) * F::kScaleBytesPerToken + head * F::kBlocksPerHead +
                 part * kBlocks;
   if constexpr (kBlocks == 8) {
@@ -356,11 +364,6 @@ __device__ __forceinline__ void fp4_store(const uint64_t* p, int row, int head, 
     static_assert(kBlocks == 2, "scale bytes per call");
     *reinterpret_cast<uint16_t*>(sf) = static_cast<uint16_t>(sfb);
   }
-  constexpr int kChunks = kN / 16;               // 16-byte code chunks
-#pragma unroll
-  for (int t = 0; t < kChunks; ++t)
-    *reinterpret_cast<uint4*>(stage_row + (((part * kChunks + t) ^ swz) << 4)) =
-        make_uint4(codes[4 * t], codes[4 * t + 1], codes[4 * t + 2], codes[4 * t + 3]);
   if (args.q_pre != nullptr) {
     const uint64_t c2 = f2_pack(kInvSqrt128, kInvSqrt128);
     float4* pre = reinterpret_cast<float4*>(args.q_pre + static_cast<long long>(row) * kQDim + head * kHeadDim +
