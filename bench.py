@@ -18,7 +18,7 @@ writes back the outputs of earlier steps) is reported as `back_to_back`.  Also m
 BF16 [4632, 7168] (GB/s against HBM), the GEMM's own launch time (for the
 roofline), the end-to-end call iq_prepare_q_host on page-locked host
 buffers (the latent read from and the FP4 output written to host memory
-inside the timed region), decode steps replayed from a CUDA graph (1, 8, 32, 64
+inside the timed region), steps replayed from a CUDA graph (1, 8, 32, 64, 96, 128
 tokens), a token sweep (128 ... 65536), the step with each FP4 output
 variant, and the CPU oracle on a bounded sample of the same workload.
 
@@ -527,7 +527,7 @@ def run_ours(args):
     # ------------------------------------------- decode under graph replay
     # Decode steps (N(0,1) latent, random positions) captured in a CUDA graph
     # per token count and per route (the small-M swapped-operand kernel, the
-    # default for M <= 64, and the CTA-pair kernel).  Per call: a graph of 24
+    # default for M <= 128, and the CTA-pair kernel).  Per call: a graph of 24
     # calls replayed ~1000 calls' worth, once with the same W every call (hot
     # in L2, as a decode loop sees it) and once with W rotated over 24 copies
     # (302 MB, more than twice L2), so that every call reads W from HBM.  Also
@@ -560,7 +560,7 @@ def run_ours(args):
         return a.elapsed_time(b) * 1e3 / (reps * len(calls))
 
     decode = {"default_route_max_tokens": iq.small_m_threshold()}
-    for Md in (1, 8, 32, 64):
+    for Md in (1, 8, 32, 64, 96, 128):
         xd, _, _, pd = W.decode_chain(Md)
         lat_d = torch.from_numpy(xd.view(np.int16)).view(torch.bfloat16).to(dev)
         pos_d = torch.from_numpy(pd).to(dev)

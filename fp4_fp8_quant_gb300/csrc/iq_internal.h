@@ -19,7 +19,7 @@ constexpr int kHeadDim = 128;
 constexpr int kQDim = kNumHeads * kHeadDim;   // 8192
 constexpr int kNumKBlocks = kLatentDim / 128; // 12
 constexpr int kScaleGroups = kNumKBlocks / 4; // 3 packed int32 words per row
-constexpr int kSmallMMax = 64;                // most tokens the small-M kernel takes
+constexpr int kSmallMMax = 128;               // most tokens the small-M kernel takes
 
 // FP4 output variants (compile-time parameter of the fused GEMM kernels).
 //   kFp4Mx:    1x32 blocks, UE8M0 scale 2^e with e the smallest integer with
@@ -122,7 +122,7 @@ cudaError_t launch_gemm_wait_selftest(const CUtensorMap& tm_x, const CUtensorMap
                                       const GemmArgs& args, int max_pairs, cudaStream_t stream);
 
 // The small-M (swapped-operand) kernel: M <= kSmallMMax tokens, one launch
-// of 64 clusters of two CTAs (one per K half).
+// of 64 clusters of two CTAs (one per K half); 64 or 128 token columns.
 cudaError_t small_m_setup_device();
 cudaError_t launch_small_m_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const GemmArgs& args,
                                              int fp4_format, cudaStream_t stream);

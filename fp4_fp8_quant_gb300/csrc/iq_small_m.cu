@@ -1,4 +1,4 @@
-// K3: the fused indexer-Q projection for few tokens (M <= 64), with the MMA
+// K3: the fused indexer-Q projection for few tokens (M <= 128), with the MMA
 // operands swapped: the weights are the MMA's M side and the tokens its N side.
 //
 // The TensorRT-LLM PR "Fuse DeepSeek-V4 Indexer Q projection with CuTe DSL"
@@ -13,17 +13,19 @@
 // MMAs and run its epilogue on a whole 256-row tile.  Here:
 //   * one cluster of two CTAs per head (128 CTAs).  Each CTA multiplies the
 //     head's 128 rows of W (the MMA's A side, M = 128) by the token rows (the
-//     B side, N = 64) over one half of K
-//     (6 of the 12 K-blocks) with the 1-SM MMA (tcgen05 kind::mxf8f6f4
-//     block_scale); the accumulators are FP32 in tensor memory;
+//     B side: N = M rounded up to 16) over one half of K (6 of the 12
+//     K-blocks) with the 1-SM MMA (tcgen05 kind::mxf8f6f4 block_scale); the
+//     accumulators are FP32 in tensor memory.  Two instances: 64 token
+//     columns for M <= 64 and 128 for 65 <= M <= 128, whose split-K exchange
+//     buffer takes the place of the first two W and token stages (K3Layout);
 //   * several MMA issuers: with one issuing thread the 24 MMAs of a CTA (32
 //     cycles of tensor work each at N = 64) measured 100-160 cycles apart;
 //     with the K-blocks dealt to three threads, each accumulating into its
-//     own 64 TMEM columns, the whole MMA phase took a third of the time.  The
+//     own TMEM columns, the whole MMA phase took a third of the time.  The
 //     epilogue adds the three partial sums;
-//   * the token tile of a K-block is loaded as exactly M rows: rows M..63 of
+//   * the token tile of a K-block is loaded as exactly M rows: rows M..N-1 of
 //     the B side keep whatever shared memory held, which reaches only
-//     accumulator columns M..63 (column n depends on B row n alone), and
+//     accumulator columns M..N-1 (column n depends on B row n alone), and
 //     those columns are never read.  (A box reaching past M would make TMA
 //     fill the missing rows, measured to delay the load by ~0.7 us at M = 1);
 //   * each CTA's share of W (96 KB) is loaded before the kernel waits for the
@@ -31,29 +33,31 @@
 //     stream serialization): W does not depend on it, so its read overlaps
 //     the quantizer;
 //   * split-K exchange through distributed shared memory: token t is finished
-//     by the CTA of K half t % 2, which receives both halves' partial sums of
-//     its tokens as asynchronous stores (st.async) counted on one of its
-//     mbarriers;
+//     by the CTA of K half t % 2, which keeps its own half's partial sums and
+//     receives the other half's as asynchronous stores (st.async) counted on
+//     one of its mbarriers;
 //   * per token one warp runs the epilogue for the head: lane l holds dims
 //     4l..4l+3, RoPE pairs (i, i+32) meet through one shuffle, the two
 //     lowest Hadamard stages run in registers and the five others across
 //     lanes with shuffles, each FP4 block of 32 dims is 8 lanes, and every
 //     lane writes its 2 code bytes, so a warp stores the head's 64 code bytes
-//     of the token at once.  A warp takes its two tokens together, so their
+//     of the token at once.  A warp takes its tokens two at a time, so their
 //     shuffle and sincos latencies overlap.
 //
 // Scale factors, as in the large-M kernel: the MMA applies one UE8M0 scale
 // per 32 K per row; the instruction descriptor's scale-ID field (kb % 4)
 // picks the byte of the packed word that holds K-block kb.  SFA carries the
 // head's weight-block scale (the same for its 128 rows), SFB the scales of the
-// 64 token rows.
+// token rows.
 //
 // Every mbarrier wait is bounded (GemmArgs::timeout_ns); a wait that gives up
 // records its kind in this kernel's device status word.  No thread leaves a
 // loop or the kernel early, so every thread of both CTAs reaches both uses of
-// the cluster barrier exactly once: arrive after set-up, wait before the
-// exchange (the peer is running); arrive after the exchange, wait at the end
-// (the peer has issued its stores into this CTA, even when a wait gave up).
+// the cluster barrier exactly once: arrive after set-up (128 columns: once
+// this CTA's MMAs on the exchange buffer's stages have completed), wait before
+// the exchange (the peer is running); arrive after the exchange, wait at the
+// end (the peer has issued its stores into this CTA, even when a wait gave
+// up).
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -70,67 +74,100 @@ __device__ uint32_t g_iq_status_small_m;
 
 namespace {
 
-constexpr int kN = kSmallMMax;                      // token columns of the MMA
 constexpr int kSplit = 2;                           // K halves: the CTAs of a cluster
 constexpr int kKbPerCta = kNumKBlocks / kSplit;     // 6
 constexpr int kWBytes = kHeadDim * 128;             // one head x one K-block: 16 KB
-constexpr int kXBytes = kN * 128;                   // 64 tokens x one K-block: 8 KB
-constexpr int kSlots = kN / kSplit;                 // tokens finished per CTA
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTokPerWarp = kSlots / kWarps;        // tokens a warp finishes in step (3)
 // MMA issuers (see above): issuer q takes K-blocks q, q + kIssuers, ... into
 // accumulator q.
 constexpr int kIssuers = 3;
 constexpr int kKbPerIssuer = kKbPerCta / kIssuers;
-constexpr uint32_t kAccCol = 0;                     // kIssuers x 64 columns
-constexpr uint32_t kSfaCol = kIssuers * kN;         // + 8 g, 4 columns each
-constexpr uint32_t kSfbCol = kSfaCol + 32;          // + 8 g, 4 columns each
-constexpr uint32_t kTmemCols = kSfbCol + 32 <= 128 ? 128 : (kSfbCol + 32 <= 256 ? 256 : 512);
-static_assert(kKbPerCta % kIssuers == 0 && kIssuers <= 6 && kSfbCol + 32 <= 512, "issuers");
+constexpr uint32_t kAccCol = 0;                     // kIssuers x kN columns
+constexpr int kNumBars = 2 * kKbPerCta + 5;
+static_assert(kKbPerCta % kIssuers == 0 && kIssuers <= 6, "issuers");
 
-// Shared-memory map (offsets from a 1024-byte aligned base).
-constexpr int kOffW = 0;
-constexpr int kOffX = kOffW + kKbPerCta * kWBytes;
-constexpr int kOffSfa = kOffX + kKbPerCta * kXBytes;
-constexpr int kOffSfb = kOffSfa + kScaleGroups * 128 * 4;
-constexpr int kOffRed = kOffSfb + kScaleGroups * 128 * 4;   // float [2 K halves][32 slots][128 dims]
-constexpr int kRedBytes = kSplit * kSlots * kHeadDim * 4;
-constexpr int kOffBar = kOffRed + kRedBytes;
-constexpr int kNumBars = 2 * kKbPerCta + 4;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+// Token columns kN of the MMA: 64 (M <= 64) or 128 (65 <= M <= 128).
+template <int kN>
+struct K3Layout {
+  static constexpr int kXBytes = kN * 128;                 // kN tokens x one K-block: 8 or 16 KB
+  static constexpr int kSlots = kN / kSplit;               // tokens finished per CTA
+  static constexpr int kTokPerWarp = kSlots / kWarps;      // tokens a warp finishes in step (3)
+  static constexpr int kCols = kN / (kWarps / 4);          // token columns a warp drains in steps (1) and (2)
+  static constexpr uint32_t kSfaCol = kIssuers * kN;       // + 8 g, 4 columns each
+  static constexpr uint32_t kSfbCol = kSfaCol + 32;        // + 8 g, 4 columns each
+  static constexpr uint32_t kTmemCols = kSfbCol + 32 <= 128 ? 128 : (kSfbCol + 32 <= 256 ? 256 : 512);
+  // The split-K exchange buffer: per K half h, float [kSlots][128 dims] (the
+  // partial sums of this CTA's tokens from half h).  With 128 token columns,
+  // W (96 KB), the tokens (96 KB) and a separate 64 KB buffer do not fit, so
+  // half 0 takes the place of the first kRedStages W stages and half 1 that of
+  // the first kRedStages token stages: the MMAs of those K-blocks are issued
+  // first, and each CTA arrives on the cluster barrier once its own have
+  // completed, so neither CTA stores into the other before both are done
+  // with those stages.
+  static constexpr bool kRedInStages = kN > 64;
+  static constexpr int kRedStages = 2;
+  static constexpr int kRedHalfBytes = kSlots * kHeadDim * 4;
+  // Shared-memory map (offsets from a 1024-byte aligned base).
+  static constexpr int kOffW = 0;
+  static constexpr int kOffX = kOffW + kKbPerCta * kWBytes;
+  static constexpr int kOffSfa = kOffX + kKbPerCta * kXBytes;
+  static constexpr int kOffSfb = kOffSfa + kScaleGroups * 128 * 4;
+  static constexpr int kOffRed0 = kRedInStages ? kOffW : kOffSfb + kScaleGroups * 128 * 4;
+  static constexpr int kOffRed1 = kRedInStages ? kOffX : kOffRed0 + kRedHalfBytes;
+  static constexpr int kOffBar = kRedInStages ? kOffSfb + kScaleGroups * 128 * 4 : kOffRed1 + kRedHalfBytes;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
 
-static_assert(kOffX % 1024 == 0 && kXBytes % 1024 == 0, "swizzled operand tiles need 1024-byte alignment");
-static_assert(kOffSfa % 16 == 0 && kOffSfb % 16 == 0 && kOffRed % 16 == 0 && kOffBar % 8 == 0, "alignment");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-static_assert(kSlots % kWarps == 0 && kIssuers + 2 <= kWarps + 1, "warp roles");
+  static_assert(kN == 64 || kN == 128, "token columns");
+  static_assert(kSfbCol + 32 <= 512, "tensor memory");
+  static_assert(kOffX % 1024 == 0 && kXBytes % 1024 == 0, "swizzled operand tiles need 1024-byte alignment");
+  static_assert(kOffSfa % 16 == 0 && kOffSfb % 16 == 0 && kOffRed0 % 16 == 0 && kOffRed1 % 16 == 0 &&
+                    kOffBar % 8 == 0,
+                "alignment");
+  // The stages that hold the buffer are K-blocks 0 .. kRedStages - 1, the
+  // first K-block of issuers 0 .. kRedStages - 1.
+  static_assert(!kRedInStages || (kRedHalfBytes <= kRedStages * kWBytes && kRedHalfBytes <= kRedStages * kXBytes &&
+                                  kRedStages <= kIssuers),
+                "exchange buffer inside the first stages");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kSlots % kWarps == 0 && kIssuers + 2 <= kWarps + 1, "warp roles");
+  static_assert(kCols == 16 || kCols == 32, "16- or 32-column tensor-memory loads");
+};
 
 __device__ __forceinline__ void fail(volatile uint32_t* abort_flag, uint32_t bit) {
   atomicOr(&g_iq_status_small_m, bit);
   *abort_flag = 1u;
 }
 
-template <int kFmt>
+template <int kFmt, int kN>
 __global__ void __launch_bounds__(kThreads, 1)
     small_m_rope_hadamard_fp4_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                                      const __grid_constant__ GemmArgs args) {
+  using L = K3Layout<kN>;
+  constexpr int kXBytes = L::kXBytes;
+  constexpr int kTokPerWarp = L::kTokPerWarp;
+  constexpr uint32_t kSfaCol = L::kSfaCol;
+  constexpr uint32_t kSfbCol = L::kSfbCol;
+  constexpr uint32_t kTmemCols = L::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sW = smem + kOffW;
-  uint8_t* sX = smem + kOffX;
-  uint32_t* sSfa = reinterpret_cast<uint32_t*>(smem + kOffSfa);
-  uint32_t* sSfb = reinterpret_cast<uint32_t*>(smem + kOffSfb);
-  float* red = reinterpret_cast<float*>(smem + kOffRed);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint8_t* sW = smem + L::kOffW;
+  uint8_t* sX = smem + L::kOffX;
+  uint32_t* sSfa = reinterpret_cast<uint32_t*>(smem + L::kOffSfa);
+  uint32_t* sSfb = reinterpret_cast<uint32_t*>(smem + L::kOffSfb);
+  float* red0 = reinterpret_cast<float*>(smem + L::kOffRed0);   // K half 0's partial sums of this CTA's tokens
+  float* red1 = reinterpret_cast<float*>(smem + L::kOffRed1);   // K half 1's
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* w_full = bars;                       // K-block i of W landed
   uint64_t* x_full = bars + kKbPerCta;           // K-block i of the tokens landed
   uint64_t* sf_full = bars + 2 * kKbPerCta;      // scale factors staged in shared memory
   uint64_t* sf_copied = sf_full + 1;             // scale factors copied into tensor memory
   uint64_t* mma_done = sf_full + 2;              // every issuer's MMAs completed
   uint64_t* red_full = sf_full + 3;              // both K halves' partial sums of this CTA's tokens landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
+  uint64_t* first_done = sf_full + 4;            // the MMAs on the exchange buffer's stages completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kOffMisc + 4);
 
   // The next kernel of the stream may be scheduled now (it waits for this
   // one's completion before it touches memory).
@@ -154,12 +191,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sf_copied, 1);
     mbar_init(mma_done, kIssuers);
     mbar_init(red_full, 1);
+    mbar_init(first_done, L::kRedStages);
     *abort_flag = 0u;
     fence_mbar_init();
-    // This CTA finishes the tokens t < M with t % 2 == rank; each of them
-    // arrives as 128 floats from each K half.
+    // This CTA finishes the tokens t < M with t % 2 == rank; the peer's K
+    // half of each arrives as 128 floats (this CTA's own half is stored
+    // locally).
     const uint32_t own_tokens = static_cast<uint32_t>((M - static_cast<int>(rank) + 1) / 2);
-    mbar_arrive_expect_tx(red_full, own_tokens * kSplit * kHeadDim * 4u);
+    mbar_arrive_expect_tx(red_full, own_tokens * kHeadDim * 4u);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -170,8 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   // This CTA is running: the peer may address its shared memory once it has
-  // passed the matching wait (just before the split-K exchange).
-  cluster_arrive_relaxed();
+  // passed the matching wait (just before the split-K exchange).  With the
+  // exchange buffer in the first stages the arrive comes once this CTA's
+  // MMAs on them have completed.
+  if constexpr (!L::kRedInStages) cluster_arrive_relaxed();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -222,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp == 1 ? 0 : warp - 2;
     if (lane == 0) {
       bool ok = true;
+      bool first_sent = false;   // this issuer's arrival on first_done
       if (q == 0) {
         ok = mbar_wait(sf_full, 0, timeout);
         if (ok) {
@@ -240,10 +282,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint64_t adesc0 = smem_desc_sw128(smem_u32(sW));
         const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sX));
-        const uint32_t idesc0 = idesc_mxf8_e4m3(kHeadDim, kN, 0, 0);
+        // The MMA's N: the token count rounded up to 16 (the step of N at
+        // M = 128); accumulator columns past it are not written, and the
+        // epilogue reads only columns below M.
+        const int n_cols = min(kN, max(16, (M + 15) & ~15));
+        const uint32_t idesc0 = idesc_mxf8_e4m3(kHeadDim, n_cols, 0, 0);
         const uint32_t acc = tmem + kAccCol + static_cast<uint32_t>(q * kN);
         for (int n = 0; n < kKbPerIssuer; ++n) {
           const int i = q + n * kIssuers;
+          // This issuer's first K-block is done with: its completion frees the
+          // exchange buffer's stages (see K3Layout).
+          if (L::kRedInStages && n == 1 && q < L::kRedStages) {
+            tc_commit(first_done);
+            first_sent = true;
+          }
           if (!mbar_wait(&w_full[i], 0, timeout) || !mbar_wait(&x_full[i], 0, timeout)) {
             ok = false;
             break;
@@ -263,6 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) fail(abort_flag, kStatusMmaWait);
+      // A wait that gave up may have left first_done without this issuer's
+      // arrival; add it (it arrives once whatever was issued has completed).
+      if (L::kRedInStages && q < L::kRedStages && !first_sent) tc_commit(first_done);
       // Arrives once everything this thread issued has completed (also when
       // a wait gave up before any MMA was issued).
       tc_commit(mma_done);
@@ -320,48 +375,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // (1) This CTA's partial sums over its K half: TMEM lane d = dim d of the
-  // head, column j of accumulator q = token j.  Warp w reads lanes
-  // 32 (w % 4).. and tokens 16 (w / 4)..
+  // head, column j of accumulator q = token j.
+  if constexpr (L::kRedInStages) {
+    // This CTA's MMAs no longer read the exchange buffer's stages: the peer
+    // may store into them once it has passed the matching wait.  The arrive
+    // publishes no data, only that the wait above has returned, so it is
+    // relaxed (a release arrive here measured ~0.75 us).
+    if (!mbar_wait(first_done, 0, timeout)) fail(abort_flag, kStatusEpilogueWait);
+    __syncwarp();
+    cluster_arrive_relaxed();
+  }
   const bool got = mbar_wait(mma_done, 0, timeout);
   if (!got) fail(abort_flag, kStatusEpilogueWait);
   __syncwarp();   // the lanes left the polling loop separately; tcgen05.ld is .sync.aligned
   tc_fence_after_sync();
+  // Warp w drains TMEM lanes 32 (w % 4).. and the 16-column chunks
+  // w / 4, w / 4 + 4, ... (token columns 16 c .. 16 c + 15 of chunk c), so
+  // that with fewer tokens than columns every warp still takes a share.
   const int quad = warp & 3;
-  constexpr int kCols = kN / (kWarps / 4);   // tokens per warp in steps (1) and (2)
-  static_assert(kCols == 16, "16-column tensor-memory loads");
-  const int col0 = (warp >> 2) * kCols;
+  constexpr int kCols = L::kCols;
+  constexpr int kChunks = kCols / 16;
+  const int chunk0 = warp >> 2;
   const int d = quad * 32 + lane;
   float v[kCols];
-  const bool have = col0 < M;   // warp-uniform
-  if (have) {
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kAccCol + static_cast<uint32_t>(col0);
-    tmem_ld_32x32b_x16(taddr, v);
-    tmem_ld_wait16(v);
+  {
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kAccCol;
+    // Per chunk that holds a token: the three accumulators' loads issued
+    // together, then one wait.
+    static_assert(kIssuers == 3, "three accumulators per chunk");
 #pragma unroll
-    for (int q = 1; q < kIssuers; ++q) {
-      float u[kCols];
-      tmem_ld_32x32b_x16(taddr + static_cast<uint32_t>(q * kN), u);
-      tmem_ld_wait16(u);
+    for (int k = 0; k < kChunks; ++k) {
+      const int c0 = 16 * (chunk0 + 4 * k);
+      if (c0 >= M) break;   // warp-uniform; chunks fill in order
+      float w[48];
 #pragma unroll
-      for (int j = 0; j < kCols; ++j) v[j] += u[j];
+      for (int q = 0; q < kIssuers; ++q) tmem_ld_32x32b_x16(taddr + static_cast<uint32_t>(q * kN + c0), w + 16 * q);
+      tmem_ld_wait(w);
+      tmem_ld_wait16(w + 32);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[16 * k + j] = w[j] + w[16 + j] + w[32 + j];
     }
   }
   tc_fence_before_sync();
 
   // (2) Split-K exchange.  Token t is finished in slot t / 2 by CTA t % 2;
-  // this CTA's partial goes to row `rank` of that CTA's red[2][32][128] as
-  // asynchronous stores counted on that CTA's red_full barrier (no
-  // cluster-scope release fence, which costs ~1K cycles here).
-  cluster_wait();   // the peer is running (its barriers are initialized)
-  const uint32_t red_here = smem_u32(red) + static_cast<uint32_t>((static_cast<int>(rank) * kSlots * kHeadDim + d) * 4);
-  const uint32_t red_to[2] = {mapa_shared(red_here, 0), mapa_shared(red_here, 1)};
-  const uint32_t bar_to[2] = {mapa_shared(smem_u32(red_full), 0), mapa_shared(smem_u32(red_full), 1)};
-  if (have) {
+  // this CTA's partial goes to that CTA's buffer of K half `rank`: for its
+  // own tokens by plain shared-memory stores (visible after the block
+  // barrier below), for the peer's as asynchronous stores counted on the
+  // peer's red_full barrier (no cluster-scope release fence, which costs ~1K
+  // cycles here).
+  cluster_wait();   // the peer is running (its barriers are initialized; with
+                    // the buffer in the first stages, its MMAs on them
+                    // have completed)
+  float* red_own = rank == 0 ? red0 : red1;
+  const uint32_t peer = rank ^ 1u;
+  const uint32_t red_peer = mapa_shared(smem_u32(red_own) + static_cast<uint32_t>(d * 4), peer);
+  const uint32_t bar_peer = mapa_shared(smem_u32(red_full), peer);
 #pragma unroll
-    for (int j = 0; j < kCols; ++j) {
-      const int t = col0 + j;   // col0 is even: t % 2 == j % 2
-      if (t < M)
-        st_async_cluster_f32(red_to[j & 1] + static_cast<uint32_t>((t >> 1) * kHeadDim * 4), v[j], bar_to[j & 1]);
+  for (int k = 0; k < kChunks; ++k) {
+    const int c0 = 16 * (chunk0 + 4 * k);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int t = c0 + j;   // c0 is even: t % 2 == j % 2
+      if (t < M) {
+        if (static_cast<uint32_t>(j & 1) == rank)
+          red_own[(t >> 1) * kHeadDim + d] = v[16 * k + j];
+        else
+          st_async_cluster_f32(red_peer + static_cast<uint32_t>((t >> 1) * kHeadDim * 4), v[16 * k + j], bar_peer);
+      }
     }
   }
   const bool red_ok = mbar_wait(red_full, 0, timeout);
@@ -378,36 +459,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // (3) Per token one warp: lane l holds dims 4l..4l+3 of the head.  A warp
-  // takes its kTokPerWarp tokens (slots warp, warp + kWarps, ...) together, so the
-  // shuffle and sincos latencies of one token overlap those of the others.
-  float x[kTokPerWarp][4];
+  // takes its tokens (slots warp, warp + kWarps, ...) two at a time, so the
+  // shuffle and sincos latencies of one token overlap those of the other.
+  // Slots fill in order, so a pair whose first slot holds no token ends the
+  // warp's work.
+  constexpr int kLanesPerBlock = Fp4Layout<kFmt>::kBlock / 4;
+  static_assert(kTokPerWarp % 2 == 0, "token pairs");
 #pragma unroll
-  for (int j = 0; j < kTokPerWarp; ++j) {
-    const int u = warp + j * kWarps;
-    const float4 a = reinterpret_cast<const float4*>(red + u * kHeadDim)[lane];
-    const float4 b = reinterpret_cast<const float4*>(red + (kSlots + u) * kHeadDim)[lane];
-    x[j][0] = a.x + b.x;
-    x[j][1] = a.y + b.y;
-    x[j][2] = a.z + b.z;
-    x[j][3] = a.w + b.w;
-  }
-  if (tok_valid[0]) {   // warp-uniform; token j is valid only if token 0 is
+  for (int g = 0; g < kTokPerWarp; g += 2) {
+    if (!tok_valid[g]) break;   // warp-uniform
+    float x[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int u = warp + (g + j) * kWarps;
+      const float4 a = reinterpret_cast<const float4*>(red0 + u * kHeadDim)[lane];
+      const float4 b = reinterpret_cast<const float4*>(red1 + u * kHeadDim)[lane];
+      x[j][0] = a.x + b.x;
+      x[j][1] = a.y + b.y;
+      x[j][2] = a.z + b.z;
+      x[j][3] = a.w + b.w;
+    }
     // NeoX RoPE on dims 0..63 (lanes 0..15): x1' = x1 c - x2 s, x2' = x2 c + x1 s.
 #pragma unroll
-    for (int j = 0; j < kTokPerWarp; ++j) {
+    for (int j = 0; j < 2; ++j) {
       float y[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) y[k] = __shfl_xor_sync(0xFFFFFFFFu, x[j][k], 8);
       if (lane < 16) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) x[j][k] = __fmaf_rn(x[j][k], rcos[j][k], __fmul_rn(y[k], rsin[j][k]));
+        for (int k = 0; k < 4; ++k) x[j][k] = __fmaf_rn(x[j][k], rcos[g + j][k], __fmul_rn(y[k], rsin[g + j][k]));
       }
     }
     // Fast Walsh-Hadamard transform in Sylvester order (unscaled): dim bits 0
     // and 1 inside the lane, bits 2..6 across lanes (partner lane l ^ m; the
     // lane with the bit clear keeps a + b, the other a - b).
 #pragma unroll
-    for (int j = 0; j < kTokPerWarp; ++j) {
+    for (int j = 0; j < 2; ++j) {
       const float h0 = x[j][0] + x[j][1], h1 = x[j][0] - x[j][1];
       const float h2 = x[j][2] + x[j][3], h3 = x[j][2] - x[j][3];
       x[j][0] = h0 + h2;
@@ -419,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int m = 1; m < 32; m <<= 1) {
       const float sg = (lane & m) ? -1.f : 1.f;
 #pragma unroll
-      for (int j = 0; j < kTokPerWarp; ++j) {
+      for (int j = 0; j < 2; ++j) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float p = __shfl_xor_sync(0xFFFFFFFFu, x[j][k], m);
@@ -429,20 +516,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // FP4 of z = v / sqrt(128): a block of 32 dims is lanes 8b..8b+7 (MX
     // variants), a block of 16 dims lanes 4b..4b+3 (NVFP4-style).
-    constexpr int kLanesPerBlock = Fp4Layout<kFmt>::kBlock / 4;
-    float amax[kTokPerWarp];
+    float amax[2];
 #pragma unroll
-    for (int j = 0; j < kTokPerWarp; ++j)
+    for (int j = 0; j < 2; ++j)
       amax[j] = fmaxf(fmaxf(fabsf(x[j][0]), fabsf(x[j][1])), fmaxf(fabsf(x[j][2]), fabsf(x[j][3])));
 #pragma unroll
     for (int m = 1; m < kLanesPerBlock; m <<= 1) {
 #pragma unroll
-      for (int j = 0; j < kTokPerWarp; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], m));
+      for (int j = 0; j < 2; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xFFFFFFFFu, amax[j], m));
     }
 #pragma unroll
-    for (int j = 0; j < kTokPerWarp; ++j) {
-      if (!tok_valid[j]) continue;   // warp-uniform
-      const long long t = tok_index[j];
+    for (int j = 0; j < 2; ++j) {
+      if (!tok_valid[g + j]) continue;   // warp-uniform
+      const long long t = tok_index[g + j];
       uint32_t codes, sbyte;
       if constexpr (kFmt != kFp4Nv) {
         const int e = fp4_block_exponent<kFmt>(amax[j] * kInvSqrt128);
@@ -481,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 }
 
-cudaLaunchConfig_t small_m_config(cudaLaunchAttribute* attr, cudaStream_t stream) {
+cudaLaunchConfig_t small_m_config(cudaLaunchAttribute* attr, int smem_bytes, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kSplit;
   attr[0].val.clusterDim.y = 1;
@@ -491,35 +577,51 @@ cudaLaunchConfig_t small_m_config(cudaLaunchAttribute* attr, cudaStream_t stream
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kNumHeads * kSplit, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cfg;
 }
 
-}  // namespace
-
-cudaError_t small_m_setup_device() {
-  for (const void* fn : {reinterpret_cast<const void*>(small_m_rope_hadamard_fp4_kernel<kFp4Mx>),
-                         reinterpret_cast<const void*>(small_m_rope_hadamard_fp4_kernel<kFp4MxOcp>),
-                         reinterpret_cast<const void*>(small_m_rope_hadamard_fp4_kernel<kFp4Nv>)}) {
-    const cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+template <int kN>
+cudaError_t small_m_setup_width() {
+  for (const void* fn : {reinterpret_cast<const void*>(small_m_rope_hadamard_fp4_kernel<kFp4Mx, kN>),
+                         reinterpret_cast<const void*>(small_m_rope_hadamard_fp4_kernel<kFp4MxOcp, kN>),
+                         reinterpret_cast<const void*>(small_m_rope_hadamard_fp4_kernel<kFp4Nv, kN>)}) {
+    const cudaError_t err =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, K3Layout<kN>::kSmemBytes);
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;
 }
 
-cudaError_t launch_small_m_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const GemmArgs& args,
-                                             int fp4_format, cudaStream_t stream) {
+template <int kN>
+cudaError_t launch_width(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const GemmArgs& args, int fp4_format,
+                         cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = small_m_config(attr, stream);
+  const cudaLaunchConfig_t cfg = small_m_config(attr, K3Layout<kN>::kSmemBytes, stream);
   switch (fp4_format) {
-    case kFp4Mx: return cudaLaunchKernelEx(&cfg, small_m_rope_hadamard_fp4_kernel<kFp4Mx>, tm_x, tm_w, args);
-    case kFp4MxOcp: return cudaLaunchKernelEx(&cfg, small_m_rope_hadamard_fp4_kernel<kFp4MxOcp>, tm_x, tm_w, args);
-    case kFp4Nv: return cudaLaunchKernelEx(&cfg, small_m_rope_hadamard_fp4_kernel<kFp4Nv>, tm_x, tm_w, args);
+    case kFp4Mx: return cudaLaunchKernelEx(&cfg, small_m_rope_hadamard_fp4_kernel<kFp4Mx, kN>, tm_x, tm_w, args);
+    case kFp4MxOcp:
+      return cudaLaunchKernelEx(&cfg, small_m_rope_hadamard_fp4_kernel<kFp4MxOcp, kN>, tm_x, tm_w, args);
+    case kFp4Nv: return cudaLaunchKernelEx(&cfg, small_m_rope_hadamard_fp4_kernel<kFp4Nv, kN>, tm_x, tm_w, args);
     default: return cudaErrorInvalidValue;
   }
+}
+
+}  // namespace
+
+cudaError_t small_m_setup_device() {
+  const cudaError_t err = small_m_setup_width<64>();
+  return err != cudaSuccess ? err : small_m_setup_width<128>();
+}
+
+cudaError_t launch_small_m_rope_hadamard_fp4(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const GemmArgs& args,
+                                             int fp4_format, cudaStream_t stream) {
+  if (args.M < 1 || args.M > kSmallMMax) return cudaErrorInvalidValue;
+  return args.M <= 64 ? launch_width<64>(tm_x, tm_w, args, fp4_format, stream)
+                      : launch_width<128>(tm_x, tm_w, args, fp4_format, stream);
 }
 
 cudaError_t read_small_m_status(uint32_t* flags, bool reset) {

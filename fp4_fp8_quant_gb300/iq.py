@@ -18,7 +18,7 @@ LATENT_DIM = 1536
 N_HEADS = 64
 HEAD_DIM = 128
 Q_DIM = 8192
-SMALL_M_MAX = 64
+SMALL_M_MAX = 128
 
 _STATUS = {0: "IQ_OK", -1: "IQ_ERR_ARG", -2: "IQ_ERR_ALIGN", -3: "IQ_ERR_SHAPE", -4: "IQ_ERR_ARCH",
            -5: "IQ_ERR_CUDA", -6: "IQ_ERR_WORKSPACE", -7: "IQ_ERR_TIMEOUT"}

@@ -112,15 +112,16 @@ iq_status iq_debug_e2m1_codes(const float* x, long long n, uint8_t* codes, cudaS
 
 /* Token-count route of the fused GEMM (operation 2).  Calls with
  * 1 <= M <= threshold run the small-M kernel, which swaps the MMA operands
- * (the weights on the MMA's M side, the tokens on its N side), the variant the
- * TensorRT-LLM PR routes small token counts to (dispatch thresholds); larger
- * M runs the persistent CTA-pair kernel.  Both compute the same operation;
+ * (the weights on the MMA's M side, the tokens on its N side: 64 token
+ * columns up to 64 tokens, 128 above), the variant the TensorRT-LLM PR routes
+ * small token counts to (dispatch thresholds); larger M runs the persistent
+ * CTA-pair kernel.  Both compute the same operation;
  * their float32 sums may round differently, within the error the parity rules
  * of operation 2 allow.  The threshold is clamped to [0, IQ_SMALL_M_MAX]; 0
  * sends every M to the CTA-pair kernel.  The default is IQ_SMALL_M_MAX.
  * Process-wide; applies to later calls from any thread (a CUDA graph keeps
  * the route it was captured with).  Returns the previous threshold. */
-#define IQ_SMALL_M_MAX 64
+#define IQ_SMALL_M_MAX 128
 int iq_set_small_m_threshold(int max_tokens);
 
 /* The current threshold (see iq_set_small_m_threshold). */

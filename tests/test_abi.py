@@ -88,12 +88,12 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
 def test_small_m_threshold_is_clamped_and_restored(lib):
     """The token-count route switch is host state only: no device needed."""
     old = lib.iq_small_m_threshold()
-    assert old == 64
+    assert old == 128
     try:
-        assert lib.iq_set_small_m_threshold(8) == 64
+        assert lib.iq_set_small_m_threshold(8) == 128
         assert lib.iq_small_m_threshold() == 8
         lib.iq_set_small_m_threshold(1000)
-        assert lib.iq_small_m_threshold() == 64
+        assert lib.iq_small_m_threshold() == 128
         lib.iq_set_small_m_threshold(-5)
         assert lib.iq_small_m_threshold() == 0
     finally:

@@ -72,7 +72,8 @@ def test_quantizer_writes_stay_inside(cuda_device, M, K):
     assert y.intact() and s.intact()
 
 
-@pytest.mark.parametrize("M,threshold", [(1, 64), (37, 64), (64, 64), (37, 0), (65, 64), (300, 64), (4633, 64)])
+@pytest.mark.parametrize("M,threshold", [(1, 128), (37, 128), (64, 128), (37, 0), (65, 64), (65, 128), (100, 128),
+                                         (128, 128), (128, 0), (300, 128), (4633, 128)])
 def test_prepare_q_writes_stay_inside(cuda_device, M, threshold):
     iq = _iq()
     x, wq, wsf, pos = W.decode_chain(M)
@@ -100,7 +101,7 @@ def test_fp4_variant_writes_stay_inside(cuda_device, fmt):
     lat = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda()
     p = torch.from_numpy(pos).cuda()
     cols = 512 if fmt == "nv" else 256
-    for threshold in (0, 64):
+    for threshold in (0, 128):
         q = Guarded(M * 4096)
         sf = Guarded(M * cols)
         with _route(threshold):

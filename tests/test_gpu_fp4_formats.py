@@ -31,7 +31,7 @@ def _run(x, wq, wsf, pos, fmt):
 
 
 @pytest.mark.parametrize("fmt", ["mx_ocp", "nv"])
-@pytest.mark.parametrize("M", [1, 16, 64, 300, 1024])
+@pytest.mark.parametrize("M", [1, 16, 64, 100, 300, 1024])
 def test_variant_matches_oracle(cuda_device, fmt, M):
     x, wq, wsf, pos = W.chain_workload(M, seed=6000 + M, outlier_p=0.005, outlier_scale=100.0)
     q, sf, z = _run(x, wq, wsf, pos, fmt)

@@ -28,12 +28,16 @@ def _iq():
 
 @contextlib.contextmanager
 def _fusion(on):
+    """Fusion on or off, with every token count on the CTA-pair route (the
+    fused launch exists only there)."""
     iq = _iq()
     prev = iq.set_quant_fusion(on)
+    route = iq.set_small_m_threshold(0)
     try:
         yield
     finally:
         iq.set_quant_fusion(prev)
+        iq.set_small_m_threshold(route)
 
 
 def _dev(x, pos, wq, wsf):

@@ -3,8 +3,8 @@ page-locked host memory, processed in row chunks whose transfers overlap the
 computation.
 
 Its results are checked against the CPU oracle at sizes where chunks of 256
-rows leave ragged tails on both GEMM routes (a last chunk of more than 64 rows
-takes the CTA-pair kernel, one of at most 64 the small-M kernel), and byte
+rows leave ragged tails on both GEMM routes (a last chunk of more than 128
+rows takes the CTA-pair kernel, one of at most 128 the small-M kernel), and byte
 for byte against the device-buffer entry at the 4,632-token prefill size,
 where every chunk takes the CTA-pair kernel: a row's arithmetic does not
 depend on the chunk or tile it falls in.

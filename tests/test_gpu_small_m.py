@@ -1,6 +1,7 @@
 """GPU parity of the small-M route (the swapped-operand kernel that
-iq_prepare_q runs for 1 <= M <= 64 tokens) against the CPU oracle, and its
-agreement with the CTA-pair kernel at the same token counts.
+iq_prepare_q runs for 1 <= M <= 128 tokens: 64 token columns up to 64
+tokens, 128 above) against the CPU oracle, and its agreement with the CTA-pair
+kernel at the same token counts.
 
 Both routes compute the same operation; their float32 sums are formed in a
 different order (the small-M kernel splits K in two halves and adds the
@@ -48,10 +49,10 @@ def _run(x, wq, wsf, pos):
     return q.cpu().numpy(), sf.cpu().numpy(), z.cpu().numpy()
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 7, 8, 9, 17, 31, 32, 33, 48, 63, 64])
+@pytest.mark.parametrize("M", [1, 2, 3, 7, 8, 9, 17, 31, 32, 33, 48, 63, 64, 65, 66, 77, 96, 100, 127, 128])
 def test_small_m_route_matches_oracle(cuda_device, M):
     x, wq, wsf, pos = W.chain_workload(M, seed=500 + M, outlier_p=0.005, outlier_scale=100.0)
-    with _route(64):
+    with _route(128):
         q, sf, z = _run(x, wq, wsf, pos)
     oq, osf, oz = O.prepare_q(x, wq, wsf, pos)
     check_prequant(z, oz)
@@ -59,11 +60,11 @@ def test_small_m_route_matches_oracle(cuda_device, M):
     assert _iq().device_status() == 0
 
 
-@pytest.mark.parametrize("M", [1, 8, 32, 64])
+@pytest.mark.parametrize("M", [1, 8, 32, 64, 96, 128])
 def test_small_m_decode_workload(cuda_device, M):
     """The decode inputs: N(0,1) latent, random positions up to 163840."""
     x, wq, wsf, pos = W.decode_chain(M)
-    with _route(64):
+    with _route(128):
         q, sf, z = _run(x, wq, wsf, pos)
     oq, osf, oz = O.prepare_q(x, wq, wsf, pos)
     check_prequant(z, oz)
@@ -71,12 +72,12 @@ def test_small_m_decode_workload(cuda_device, M):
     assert stats["equal_fraction"] >= 0.9999
 
 
-@pytest.mark.parametrize("M", [1, 5, 64])
+@pytest.mark.parametrize("M", [1, 5, 64, 65, 128])
 def test_both_routes_agree_with_the_oracle_and_each_other(cuda_device, M):
     x, wq, wsf, pos = W.chain_workload(M, seed=900 + M, outlier_p=0.001, outlier_scale=50.0)
     oq, osf, oz = O.prepare_q(x, wq, wsf, pos)
     outs = []
-    for threshold in (0, 64):
+    for threshold in (0, 128):
         with _route(threshold):
             q, sf, z = _run(x, wq, wsf, pos)
         check_prequant(z, oz)
@@ -93,7 +94,7 @@ def test_small_m_zero_latent_and_extreme_positions(cuda_device):
     x, wq, wsf, pos = W.chain_workload(M, seed=77, outlier_p=0.0, outlier_scale=1.0)
     x[3] = 0                                   # one all-zero token
     pos = np.array([0, 1, 163839, 2 ** 23, 5, 65535, 100000, 7, 8, 9, 10, 163838], dtype=np.int32)
-    with _route(64):
+    with _route(128):
         q, sf, z = _run(x, wq, wsf, pos)
     oq, osf, oz = O.prepare_q(x, wq, wsf, pos)
     check_prequant(z, oz)
@@ -101,15 +102,15 @@ def test_small_m_zero_latent_and_extreme_positions(cuda_device):
     assert np.all((q[3] & 0x77) == 0) and np.all(sf[3] == 112)
 
 
-def test_small_m_graph_replay_and_static_entry(cuda_device):
+@pytest.mark.parametrize("M", [24, 100])
+def test_small_m_graph_replay_and_static_entry(cuda_device, M):
     """A captured small-M call replays to the eager result; the allocation-free
     entry point takes the same route."""
     iq = _iq()
     L = iq.lib()
-    M = 24
     x, wq, wsf, pos = W.decode_chain(M)
     lat, w, ws, p = _dev(x, pos, wq, wsf)
-    with _route(64):
+    with _route(128):
         work = torch.empty(iq.prepare_q_workspace_bytes(M), dtype=torch.uint8, device="cuda")
         q = torch.empty((M, 4096), dtype=torch.uint8, device="cuda")
         s = torch.empty((M, 256), dtype=torch.uint8, device="cuda")

@@ -29,11 +29,13 @@ def _tiling(tile_n, order):
     iq = _iq()
     iq.set_gemm_tiling(tile_n, order)
     prev = iq.set_quant_fusion(False)
+    route = iq.set_small_m_threshold(0)   # every M on the CTA-pair kernel
     try:
         yield
     finally:
         iq.set_gemm_tiling(0, 0)
         iq.set_quant_fusion(prev)
+        iq.set_small_m_threshold(route)
 
 
 def _dev(x, pos, wq, wsf):
