@@ -186,11 +186,12 @@ def test_device_status_word_is_clean(cuda_device):
     assert _iq().device_status() == 0
 
 
-@pytest.mark.parametrize("M", [5, 300])
+@pytest.mark.parametrize("M", [5, 100, 300])
 def test_negative_and_large_positions(cuda_device, M):
     """The header allows any position with |p| < 2^24: negative positions and
-    positions far beyond the pages' 163840 rotate like any other, on both the
-    small-M route (M = 5) and the CTA-pair route (M = 300)."""
+    positions far beyond the pages' 163840 rotate like any other, on the
+    small-M route (M = 5: 64 token columns, M = 100: 128) and the CTA-pair
+    route (M = 300)."""
     x, wq, wsf, pos = W.chain_workload(M, seed=4000 + M, outlier_p=0.001, outlier_scale=50.0)
     rng = np.random.default_rng(M)
     pos = rng.integers(-(1 << 24) + 1, 1 << 24, size=M).astype(np.int32)
