@@ -43,7 +43,7 @@ def _dev(x, pos, wq, wsf):
     return lat, torch.from_numpy(wq).cuda(), torch.from_numpy(wsf).cuda(), torch.from_numpy(pos).cuda()
 
 
-@pytest.mark.parametrize("M", [65, 100, 128, 200, 256, 512, 1024])
+@pytest.mark.parametrize("M", [65, 100, 128, 129, 200, 256, 512, 1024])
 def test_mid_size_token_counts_match_oracle(cuda_device, M):
     x, wq, wsf, pos = W.sweep_chain(M, seed=700 + M)
     lat, w, ws, p = _dev(x, pos, wq, wsf)
