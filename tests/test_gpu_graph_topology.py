@@ -60,8 +60,8 @@ def _node_types(call, stream):
         cu.cuGraphDestroy(graph)
 
 
-@pytest.mark.parametrize("M,fused,kernels", [(24, True, 2), (300, True, 1), (4632, True, 1),
-                                              (300, False, 2), (4632, False, 2)])
+@pytest.mark.parametrize("M,fused,kernels", [(24, True, 2), (100, True, 2), (300, True, 1), (4632, True, 1),
+                                              (100, False, 2), (300, False, 2), (4632, False, 2)])
 def test_captured_prepare_q_kernel_nodes(cuda_device, M, fused, kernels):
     from fp4_fp8_quant_gb300 import iq
     prev = iq.set_quant_fusion(fused)
