@@ -942,9 +942,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait(v + 32);
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(tmem_empty_leader0 + 8u * static_cast<uint32_t>(acc));
+        // The pair's last tile needs no release: nothing waits for it, and
+        // without this remote arrive no cluster access of this CTA is left in
+        // flight at the final cluster barrier (see there).
+        if (lane == 0 && local != my_count - 1)
+          mbar_arrive_remote(tmem_empty_leader0 + 8u * static_cast<uint32_t>(acc));
         if (!kFuse && local == my_count - 1) {
-          cluster_arrive_release();
+          cluster_arrive_relaxed();
           cluster_arrived = true;
         }
         // The last stage (dim bit 6): a + b in the first half, a - b in the
@@ -973,7 +977,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The accumulator values are in registers (tcgen05.wait::ld above), so
         // the leader may overwrite it: a CTA-scope arrive suffices and does not
         // wait for earlier global stores to reach L2.
-        if (lane == 0) mbar_arrive_remote(tmem_empty_leader0 + 8u * static_cast<uint32_t>(acc));
+        if (lane == 0 && local != my_count - 1)   // none for the last tile (see the one-head path)
+          mbar_arrive_remote(tmem_empty_leader0 + 8u * static_cast<uint32_t>(acc));
         uint64_t p[64];
 #pragma unroll
         for (int j = 0; j < 64; ++j) p[j] = f2_pack(v[2 * j], v[2 * j + 1]);
@@ -999,14 +1004,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // Neither CTA leaves (or frees tensor memory) while the pair may still use
-  // its shared memory, barriers or tensor memory.  With one-head tiles the
-  // epilogue warps arrive as soon as their last accumulator read and remote
-  // arrive are done: a release arrive after the tile's output stores would
-  // wait for those to reach memory (~0.5 us of a ~9 us call at 128 tokens),
-  // and nothing in the other CTA depends on them.  (With two-head tiles the
-  // early arrive measured ~1 % slower at 4632 tokens.)
+  // its shared memory, barriers or tensor memory.  Every access of one CTA to
+  // the other's shared memory has been seen to complete by then (loads and
+  // MMAs through the stage and final barriers, scale-staging arrives through
+  // the issuer's waits, accumulator releases through the issuer's waits, and
+  // the last tile sends none), so the arrive publishes nothing and is
+  // relaxed: a release arrive waited for this CTA's outstanding stores
+  // (~0.2 us per call at 256 and 512 tokens).  With one-head tiles the
+  // epilogue warps arrive as soon as their last accumulator read is done.
+  // (With two-head tiles that early arrive, then a release, measured ~1 %
+  // slower at 4632 tokens.)
   tc_fence_before_sync();
-  if (!cluster_arrived) cluster_arrive_release();
+  if (!cluster_arrived) cluster_arrive_relaxed();
   cluster_wait();
   if (warp == 1) {
     tc_fence_after_sync();
