@@ -39,7 +39,8 @@
 // histograms in shared memory; a row of up to 12288 keys is read once and
 // kept in shared memory), then a pass in index order over contiguous
 // per-thread segments that writes the keys above the threshold and the first
-// (smallest-index) keys equal to it.
+// (smallest-index) keys equal to it.  Every sweep takes four keys per access
+// when the row is 16-byte aligned.
 //
 // Every mbarrier wait is bounded (timeout_ns); a wait that gives up records
 // its kind in this file's status word and raises a CTA abort flag.
@@ -544,7 +545,7 @@ __device__ uint32_t find_digit(const uint32_t* hist, int nb, uint32_t rank, uint
 // file comment).  Rows of at most kTopkCacheMax visible keys are read from
 // global memory once, as order-preserving keys into shared memory; longer
 // rows are read again by every pass.
-__global__ void __launch_bounds__(kTopkThreads)
+__global__ void __launch_bounds__(kTopkThreads, 8)
     indexer_topk_kernel(const float* logits, long long ld, int N, const int32_t* len, int k,
                         int32_t* __restrict__ out, int cache_keys) {
   extern __shared__ uint32_t cache[];   // cache_keys words
@@ -565,11 +566,40 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
   const bool cached = L <= cache_keys;
   auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : score_key(row[i]); };
+  // Four keys per access where the row is 16-byte aligned (16-byte loads of
+  // the scores and of the cache); the last L % 4 keys, or every key of an
+  // unaligned row, one at a time.  Every pass visits each key exactly once.
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0u;
+  const int L4 = vec ? L >> 2 : 0;
+  auto quad_at = [&](int q) -> uint4 {
+    if (cached) return reinterpret_cast<const uint4*>(cache)[q];
+    const float4 f = reinterpret_cast<const float4*>(row)[q];
+    return make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
+  };
+  auto for_each_key = [&](auto&& fn) {
+    for (int q = threadIdx.x; q < L4; q += kTopkThreads) {
+      const uint4 kk = quad_at(q);
+      fn(kk.x);
+      fn(kk.y);
+      fn(kk.z);
+      fn(kk.w);
+    }
+    for (int i = 4 * L4 + threadIdx.x; i < L; i += kTopkThreads) fn(key_at(i));
+  };
 
   // Digit 1: bits 31..21 (read the row, cache it).
   for (int i = threadIdx.x; i < 2048; i += kTopkThreads) hist[i] = 0u;
   __syncthreads();
-  for (int i = threadIdx.x; i < L; i += kTopkThreads) {
+  for (int q = threadIdx.x; q < L4; q += kTopkThreads) {
+    const float4 f = reinterpret_cast<const float4*>(row)[q];
+    const uint4 kk = make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
+    if (cached) reinterpret_cast<uint4*>(cache)[q] = kk;
+    atomicAdd(&hist[kk.x >> 21], 1u);
+    atomicAdd(&hist[kk.y >> 21], 1u);
+    atomicAdd(&hist[kk.z >> 21], 1u);
+    atomicAdd(&hist[kk.w >> 21], 1u);
+  }
+  for (int i = 4 * L4 + threadIdx.x; i < L; i += kTopkThreads) {
     const uint32_t key = score_key(row[i]);
     if (cached) cache[i] = key;
     atomicAdd(&hist[key >> 21], 1u);
@@ -580,46 +610,65 @@ __global__ void __launch_bounds__(kTopkThreads)
   // Digit 2: bits 20..10 of the keys with digit 1 = d1.
   for (int i = threadIdx.x; i < 2048; i += kTopkThreads) hist[i] = 0u;
   __syncthreads();
-  for (int i = threadIdx.x; i < L; i += kTopkThreads) {
-    const uint32_t key = key_at(i);
+  for_each_key([&](uint32_t key) {
     if ((key >> 21) == d1) atomicAdd(&hist[(key >> 10) & 0x7FFu], 1u);
-  }
+  });
   __syncthreads();
   const uint32_t d2 = find_digit(hist, 2048, static_cast<uint32_t>(k) - above1, scratch, &above2);
   // Digit 3: bits 9..0 of the keys with digits (d1, d2).
   for (int i = threadIdx.x; i < 1024; i += kTopkThreads) hist[i] = 0u;
   __syncthreads();
   const uint32_t hi22 = (d1 << 11) | d2;
-  for (int i = threadIdx.x; i < L; i += kTopkThreads) {
-    const uint32_t key = key_at(i);
+  for_each_key([&](uint32_t key) {
     if ((key >> 10) == hi22) atomicAdd(&hist[key & 0x3FFu], 1u);
-  }
+  });
   __syncthreads();
   const uint32_t d3 = find_digit(hist, 1024, static_cast<uint32_t>(k) - above1 - above2, scratch, &above3);
   const uint32_t T = (hi22 << 10) | d3;
   const uint32_t n_above = above1 + above2 + above3;            // keys > T
   const uint32_t n_equal = static_cast<uint32_t>(k) - n_above;  // keys == T to take, smallest index first
 
-  // Output: thread i takes the contiguous segment [i seg, (i + 1) seg); one
-  // scan of its counts gives where its chosen keys go.
-  const int seg = (L + kTopkThreads - 1) / kTopkThreads;
+  // Output: thread i takes the contiguous segment [i seg, (i + 1) seg) (seg a
+  // multiple of 4 when the row is aligned); one scan of its counts gives
+  // where its chosen keys go.
+  const int seg = vec ? ((L + 4 * kTopkThreads - 1) / (4 * kTopkThreads)) * 4 : (L + kTopkThreads - 1) / kTopkThreads;
   const int b = threadIdx.x * seg;
   const int e = min(L, b + seg);
   uint32_t gt = 0, eq = 0;
-  for (int i = b; i < e; ++i) {
-    const uint32_t key = key_at(i);
+  auto count = [&](uint32_t key) {
     gt += key > T ? 1u : 0u;
     eq += key == T ? 1u : 0u;
+  };
+  int i0 = b;
+  if (vec) {
+    for (; i0 + 4 <= e; i0 += 4) {
+      const uint4 kk = quad_at(i0 >> 2);
+      count(kk.x);
+      count(kk.y);
+      count(kk.z);
+      count(kk.w);
+    }
   }
+  for (int i = i0; i < e; ++i) count(key_at(i));
   uint32_t tot;
   const uint32_t gt_before = block_exclusive_scan(gt, scratch, &tot);
   uint32_t eq_before = block_exclusive_scan(eq, scratch, &tot);
   uint32_t pos = gt_before + min(eq_before, n_equal);
-  for (int i = b; i < e; ++i) {
-    const uint32_t key = key_at(i);
+  auto emit = [&](uint32_t key, int i) {
     if (key > T || (key == T && eq_before < n_equal)) dst[pos++] = i;
     if (key == T) ++eq_before;
+  };
+  i0 = b;
+  if (vec) {
+    for (; i0 + 4 <= e; i0 += 4) {
+      const uint4 kk = quad_at(i0 >> 2);
+      emit(kk.x, i0);
+      emit(kk.y, i0 + 1);
+      emit(kk.z, i0 + 2);
+      emit(kk.w, i0 + 3);
+    }
   }
+  for (int i = i0; i < e; ++i) emit(key_at(i), i);
 }
 
 }  // namespace
