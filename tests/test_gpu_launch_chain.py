@@ -149,3 +149,41 @@ def test_prepare_then_indexer_without_synchronisation(cuda_device):
     for (lg_g, top_g), (lg_w, top_w) in zip(got, want):
         assert torch.equal(lg_g, lg_w) and torch.equal(top_g, top_w)
     assert iq.device_status() == 0
+
+
+def test_mixed_routes_back_to_back(cuda_device):
+    """Calls of different token counts in a row on one stream, so that each
+    kernel's programmatic successor is another route or instance (both
+    small-M widths and the CTA-pair kernel), eager and in a captured graph;
+    every result must equal the same call made alone."""
+    iq = _iq()
+    Ms = [100, 64, 300, 1, 128, 4632, 65]
+    cases = [_inputs(M, 1, 1300 + M) for M in Ms]
+    want = [_alone(iq, lats[0], w, ws, p) for (lats, w, ws, p) in cases]
+    outs = [(torch.empty((M, 4096), dtype=torch.uint8, device="cuda"),
+             torch.empty((M, 256), dtype=torch.uint8, device="cuda")) for M in Ms]
+    works = [torch.empty(iq.prepare_q_workspace_bytes(M), dtype=torch.uint8, device="cuda") for M in Ms]
+
+    def issue():
+        for (lats, w, ws, p), (q, s), work in zip(cases, outs, works):
+            iq.prepare_q(lats[0], w, ws, p, q_fp4=q, q_sf=s, workspace=work)
+
+    issue()
+    torch.cuda.synchronize()
+    for (q, s), (qw, sw) in zip(outs, want):
+        assert torch.equal(q, qw) and torch.equal(s, sw)
+    for q, s in outs:
+        q.zero_()
+        s.zero_()
+    g = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            issue()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for (q, s), (qw, sw) in zip(outs, want):
+        assert torch.equal(q, qw) and torch.equal(s, sw)
+    assert iq.device_status() == 0
