@@ -65,12 +65,15 @@ def _topk(logits, L, k, N=None):
     return out.cpu().numpy()
 
 
+@pytest.mark.parametrize("N", [5000, 5001])
 @pytest.mark.parametrize("k", [1, 7, 64, 2048])
-def test_topk_selection_is_exact_on_given_scores(cuda_device, k):
+def test_topk_selection_is_exact_on_given_scores(cuda_device, k, N):
     """The selection on arbitrary float32 scores (many ties, +-0, -inf, wide
-    ranges) equals the oracle's selection on the same scores."""
+    ranges) equals the oracle's selection on the same scores.  N = 5001 makes
+    every row but the first start off a 16-byte boundary (the kernel's
+    one-key-per-access path), N = 5000 keeps all rows aligned."""
     rng = np.random.default_rng(k)
-    M, N = 12, 5000
+    M = 12
     s = rng.integers(-20, 20, (M, N)).astype(np.float32)                   # heavy ties
     s[1] = rng.standard_normal(N).astype(np.float32) * np.float32(1e30)
     s[2] = np.where(rng.random(N) < 0.5, np.float32(0.0), np.float32(-0.0))  # only signed zeros
