@@ -40,7 +40,8 @@
 // kept in shared memory), then a pass in index order over contiguous
 // per-thread segments that writes the keys above the threshold and the first
 // (smallest-index) keys equal to it.  Every sweep takes four keys per access
-// when the row is 16-byte aligned.
+// when the row is 16-byte aligned; rows longer than 12288 keys take 1024
+// threads and a cache of up to 49152 keys.
 //
 // Every mbarrier wait is bounded (timeout_ns); a wait that gives up records
 // its kind in this file's status word and raises a CTA abort flag.
@@ -475,6 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------- top-k
 
 constexpr int kTopkThreads = 256;
+constexpr int kTopkLongThreads = 1024;   // rows longer than the cache
+constexpr int kTopkLongCacheMax = 49152;   // the 1024-thread instance's row cache (192 KB, one CTA per SM)
 constexpr int kTopkCacheMax = 12288;   // rows up to this many keys are read once, into shared memory
 
 // Order-preserving key of a float score (larger score -> larger key); -0 is
@@ -487,6 +490,7 @@ __device__ __forceinline__ uint32_t score_key(float x) {
 
 // Block-wide exclusive prefix sum of one value per thread; returns the
 // thread's prefix and writes the block total to *total.
+template <int kThreads>
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* scratch, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
@@ -498,17 +502,17 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* s
   if (lane == 31) scratch[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t t = lane < kTopkThreads / 32 ? scratch[lane] : 0u;
+    uint32_t t = lane < kThreads / 32 ? scratch[lane] : 0u;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, t, d);
       if (lane >= d) t += y;
     }
-    if (lane < kTopkThreads / 32) scratch[lane] = t;   // inclusive over warps
+    if (lane < kThreads / 32) scratch[lane] = t;   // inclusive over warps
   }
   __syncthreads();
   const uint32_t before = warp > 0 ? scratch[warp - 1] : 0u;
-  *total = scratch[kTopkThreads / 32 - 1];
+  *total = scratch[kThreads / 32 - 1];
   __syncthreads();
   return before + x - v;
 }
@@ -516,14 +520,15 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* s
 // The digit d (of the histogram's nb bins, largest first) that holds the
 // rank-th largest of the counted keys (rank from 1), and *above = the count of
 // keys with a larger digit.
+template <int kThreads>
 __device__ uint32_t find_digit(const uint32_t* hist, int nb, uint32_t rank, uint32_t* scratch, uint32_t* above) {
   __shared__ uint32_t found_digit, found_above;
-  const int per = nb / kTopkThreads;
+  const int per = nb / kThreads;
   const int first = nb - (threadIdx.x + 1) * per;   // thread 0 takes the largest digits
   uint32_t run = 0;
   for (int j = 0; j < per; ++j) run += hist[first + j];
   uint32_t total;
-  const uint32_t before = block_exclusive_scan(run, scratch, &total);   // keys with larger digits
+  const uint32_t before = block_exclusive_scan<kThreads>(run, scratch, &total);   // keys with larger digits
   if (before < rank && rank <= before + run) {
     uint32_t acc = before;
     for (int j = per - 1; j >= 0; --j) {
@@ -542,15 +547,18 @@ __device__ uint32_t find_digit(const uint32_t* hist, int nb, uint32_t rank, uint
 }
 
 // K6: per query row t, the k visible keys with the largest scores (see the
-// file comment).  Rows of at most kTopkCacheMax visible keys are read from
+// file comment).  Rows of at most cache_keys visible keys are read from
 // global memory once, as order-preserving keys into shared memory; longer
-// rows are read again by every pass.
-__global__ void __launch_bounds__(kTopkThreads, 8)
+// rows are read again by every pass.  Two instances: 256 threads with a cache
+// of up to kTopkCacheMax keys (eight CTAs per SM), and, when the rows can be
+// longer than that, 1024 threads with a cache of up to kTopkLongCacheMax.
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads, 2048 / kThreads)
     indexer_topk_kernel(const float* logits, long long ld, int N, const int32_t* len, int k,
                         int32_t* __restrict__ out, int cache_keys) {
   extern __shared__ uint32_t cache[];   // cache_keys words
   __shared__ uint32_t hist[2048];
-  __shared__ uint32_t scratch[kTopkThreads / 32];
+  __shared__ uint32_t scratch[kThreads / 32];
   // The scores are the preceding kernel's output.  They and the lengths are
   // read through plain pointers (no __restrict__, no read-only path), so the
   // compiler keeps those loads below the wait.
@@ -561,7 +569,7 @@ __global__ void __launch_bounds__(kTopkThreads, 8)
   int L = len[t];
   L = L < 0 ? 0 : (L > N ? N : L);
   if (L <= k) {
-    for (int i = threadIdx.x; i < k; i += kTopkThreads) dst[i] = i < L ? i : -1;
+    for (int i = threadIdx.x; i < k; i += kThreads) dst[i] = i < L ? i : -1;
     return;
   }
   const bool cached = L <= cache_keys;
@@ -577,20 +585,20 @@ __global__ void __launch_bounds__(kTopkThreads, 8)
     return make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
   };
   auto for_each_key = [&](auto&& fn) {
-    for (int q = threadIdx.x; q < L4; q += kTopkThreads) {
+    for (int q = threadIdx.x; q < L4; q += kThreads) {
       const uint4 kk = quad_at(q);
       fn(kk.x);
       fn(kk.y);
       fn(kk.z);
       fn(kk.w);
     }
-    for (int i = 4 * L4 + threadIdx.x; i < L; i += kTopkThreads) fn(key_at(i));
+    for (int i = 4 * L4 + threadIdx.x; i < L; i += kThreads) fn(key_at(i));
   };
 
   // Digit 1: bits 31..21 (read the row, cache it).
-  for (int i = threadIdx.x; i < 2048; i += kTopkThreads) hist[i] = 0u;
+  for (int i = threadIdx.x; i < 2048; i += kThreads) hist[i] = 0u;
   __syncthreads();
-  for (int q = threadIdx.x; q < L4; q += kTopkThreads) {
+  for (int q = threadIdx.x; q < L4; q += kThreads) {
     const float4 f = reinterpret_cast<const float4*>(row)[q];
     const uint4 kk = make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
     if (cached) reinterpret_cast<uint4*>(cache)[q] = kk;
@@ -599,31 +607,31 @@ __global__ void __launch_bounds__(kTopkThreads, 8)
     atomicAdd(&hist[kk.z >> 21], 1u);
     atomicAdd(&hist[kk.w >> 21], 1u);
   }
-  for (int i = 4 * L4 + threadIdx.x; i < L; i += kTopkThreads) {
+  for (int i = 4 * L4 + threadIdx.x; i < L; i += kThreads) {
     const uint32_t key = score_key(row[i]);
     if (cached) cache[i] = key;
     atomicAdd(&hist[key >> 21], 1u);
   }
   __syncthreads();
   uint32_t above1, above2, above3;
-  const uint32_t d1 = find_digit(hist, 2048, static_cast<uint32_t>(k), scratch, &above1);
+  const uint32_t d1 = find_digit<kThreads>(hist, 2048, static_cast<uint32_t>(k), scratch, &above1);
   // Digit 2: bits 20..10 of the keys with digit 1 = d1.
-  for (int i = threadIdx.x; i < 2048; i += kTopkThreads) hist[i] = 0u;
+  for (int i = threadIdx.x; i < 2048; i += kThreads) hist[i] = 0u;
   __syncthreads();
   for_each_key([&](uint32_t key) {
     if ((key >> 21) == d1) atomicAdd(&hist[(key >> 10) & 0x7FFu], 1u);
   });
   __syncthreads();
-  const uint32_t d2 = find_digit(hist, 2048, static_cast<uint32_t>(k) - above1, scratch, &above2);
+  const uint32_t d2 = find_digit<kThreads>(hist, 2048, static_cast<uint32_t>(k) - above1, scratch, &above2);
   // Digit 3: bits 9..0 of the keys with digits (d1, d2).
-  for (int i = threadIdx.x; i < 1024; i += kTopkThreads) hist[i] = 0u;
+  for (int i = threadIdx.x; i < 1024; i += kThreads) hist[i] = 0u;
   __syncthreads();
   const uint32_t hi22 = (d1 << 11) | d2;
   for_each_key([&](uint32_t key) {
     if ((key >> 10) == hi22) atomicAdd(&hist[key & 0x3FFu], 1u);
   });
   __syncthreads();
-  const uint32_t d3 = find_digit(hist, 1024, static_cast<uint32_t>(k) - above1 - above2, scratch, &above3);
+  const uint32_t d3 = find_digit<kThreads>(hist, 1024, static_cast<uint32_t>(k) - above1 - above2, scratch, &above3);
   const uint32_t T = (hi22 << 10) | d3;
   const uint32_t n_above = above1 + above2 + above3;            // keys > T
   const uint32_t n_equal = static_cast<uint32_t>(k) - n_above;  // keys == T to take, smallest index first
@@ -631,7 +639,7 @@ __global__ void __launch_bounds__(kTopkThreads, 8)
   // Output: thread i takes the contiguous segment [i seg, (i + 1) seg) (seg a
   // multiple of 4 when the row is aligned); one scan of its counts gives
   // where its chosen keys go.
-  const int seg = vec ? ((L + 4 * kTopkThreads - 1) / (4 * kTopkThreads)) * 4 : (L + kTopkThreads - 1) / kTopkThreads;
+  const int seg = vec ? ((L + 4 * kThreads - 1) / (4 * kThreads)) * 4 : (L + kThreads - 1) / kThreads;
   const int b = threadIdx.x * seg;
   const int e = min(L, b + seg);
   uint32_t gt = 0, eq = 0;
@@ -651,8 +659,8 @@ __global__ void __launch_bounds__(kTopkThreads, 8)
   }
   for (int i = i0; i < e; ++i) count(key_at(i));
   uint32_t tot;
-  const uint32_t gt_before = block_exclusive_scan(gt, scratch, &tot);
-  uint32_t eq_before = block_exclusive_scan(eq, scratch, &tot);
+  const uint32_t gt_before = block_exclusive_scan<kThreads>(gt, scratch, &tot);
+  uint32_t eq_before = block_exclusive_scan<kThreads>(eq, scratch, &tot);
   uint32_t pos = gt_before + min(eq_before, n_equal);
   auto emit = [&](uint32_t key, int i) {
     if (key > T || (key == T && eq_before < n_equal)) dst[pos++] = i;
@@ -707,8 +715,11 @@ cudaError_t indexer_setup_device() {
   cudaError_t err =
       cudaFuncSetAttribute(indexer_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(indexer_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  err = cudaFuncSetAttribute(indexer_topk_kernel<kTopkThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kTopkCacheMax * static_cast<int>(sizeof(uint32_t)));
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(indexer_topk_kernel<kTopkLongThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTopkLongCacheMax * static_cast<int>(sizeof(uint32_t)));
   if (err != cudaSuccess) return err;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = logits_config(1, attr, nullptr);
@@ -756,13 +767,21 @@ cudaError_t launch_indexer_topk(const float* logits, long long ld, int M, int N,
   const int cache_keys = N < kTopkCacheMax ? N : kTopkCacheMax;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(M, 1, 1);
-  cfg.blockDim = dim3(kTopkThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(N <= kTopkCacheMax ? cache_keys : 0) * sizeof(uint32_t);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, indexer_topk_kernel, logits, ld, N, len, k, out,
-                            N <= kTopkCacheMax ? cache_keys : 0);
+  if (N > kTopkCacheMax) {
+    // Long rows: four times the threads per row (four times the loads in
+    // flight) and a row cache of up to kTopkLongCacheMax keys; longer rows
+    // are streamed from global memory by every pass.
+    const int long_cache = N <= kTopkLongCacheMax ? N : 0;
+    cfg.blockDim = dim3(kTopkLongThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(long_cache) * sizeof(uint32_t);
+    return cudaLaunchKernelEx(&cfg, indexer_topk_kernel<kTopkLongThreads>, logits, ld, N, len, k, out, long_cache);
+  }
+  cfg.blockDim = dim3(kTopkThreads, 1, 1);
+  return cudaLaunchKernelEx(&cfg, indexer_topk_kernel<kTopkThreads>, logits, ld, N, len, k, out, cache_keys);
 }
 
 cudaError_t read_indexer_status(uint32_t* flags, bool reset) {

@@ -86,11 +86,14 @@ def test_topk_selection_is_exact_on_given_scores(cuda_device, k, N):
     assert np.array_equal(got, want)
 
 
-def test_topk_long_rows_are_exact(cuda_device):
-    """Rows longer than the kernel's shared-memory row cache (12288 keys),
-    with and without ties in the first digit's threshold bin."""
+@pytest.mark.parametrize("N", [20000, 50001])
+def test_topk_long_rows_are_exact(cuda_device, N):
+    """Rows longer than the 256-thread instance's row cache (12288 keys): up to
+    49152 keys the 1024-thread instance caches them (N = 20000), beyond that
+    every pass reads them again (N = 50001, rows also off 16-byte
+    boundaries); with and without ties in the first digit's threshold bin."""
     rng = np.random.default_rng(77)
-    M, N, k = 5, 20000, 2048
+    M, k = 5, 2048
     s = rng.standard_normal((M, N)).astype(np.float32)
     s[1] = rng.integers(-3, 4, N).astype(np.float32)       # a few values: the threshold bin overflows the gather
     s[2] = np.float32(2.0)
