@@ -556,8 +556,9 @@ template <int kThreads>
 __global__ void __launch_bounds__(kThreads, 2048 / kThreads)
     indexer_topk_kernel(const float* logits, long long ld, int N, const int32_t* len, int k,
                         int32_t* __restrict__ out, int cache_keys) {
-  extern __shared__ uint32_t cache[];   // cache_keys words
-  __shared__ uint32_t hist[2048];
+  // Both are read and written with 16-byte accesses.
+  extern __shared__ __align__(16) uint32_t cache[];   // cache_keys words
+  __shared__ __align__(16) uint32_t hist[2048];
   __shared__ uint32_t scratch[kThreads / 32];
   // The scores are the preceding kernel's output.  They and the lengths are
   // read through plain pointers (no __restrict__, no read-only path), so the
@@ -662,8 +663,13 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads)
   const uint32_t gt_before = block_exclusive_scan<kThreads>(gt, scratch, &tot);
   uint32_t eq_before = block_exclusive_scan<kThreads>(eq, scratch, &tot);
   uint32_t pos = gt_before + min(eq_before, n_equal);
+  // The chosen indices (exactly k of them, positions 0..k-1) are written to
+  // the histogram buffer, free since the last digit was found, and leave in
+  // coalesced stores; with k > 2048 they go straight to their destination.
+  const bool staged = k <= 2048;
+  int32_t* sel = staged ? reinterpret_cast<int32_t*>(hist) : dst;
   auto emit = [&](uint32_t key, int i) {
-    if (key > T || (key == T && eq_before < n_equal)) dst[pos++] = i;
+    if (key > T || (key == T && eq_before < n_equal)) sel[pos++] = i;
     if (key == T) ++eq_before;
   };
   i0 = b;
@@ -677,6 +683,15 @@ __global__ void __launch_bounds__(kThreads, 2048 / kThreads)
     }
   }
   for (int i = i0; i < e; ++i) emit(key_at(i), i);
+  if (staged) {
+    __syncthreads();
+    if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0u && (k & 3) == 0) {
+      for (int q = threadIdx.x; q < (k >> 2); q += kThreads)
+        reinterpret_cast<int4*>(dst)[q] = reinterpret_cast<const int4*>(hist)[q];
+    } else {
+      for (int i = threadIdx.x; i < k; i += kThreads) dst[i] = static_cast<int32_t>(hist[i]);
+    }
+  }
 }
 
 }  // namespace
